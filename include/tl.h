@@ -1,0 +1,158 @@
+/*
+ * tl.h — C ABI of the GB300 (sm_103a) ternary linear layer library.
+ *
+ * The layer (Qiita item ecc183fae033565af7cb, "Ternary-Bonsai-2-27B on
+ * 2x RTX 5070 12GB with vLLM TP=2", sections 前提 and §4 "効いた高速化"):
+ *
+ *   weights   code[n,k] in {-1,0,+1}, one fp16 scale s[n,g] per 128 columns
+ *   rotation  xr = (1/32) H1024 x per 1024-column block (Sylvester order)
+ *   weights   smax[n] = max_g |s[n,g]|, q[n,g] = rne(127 s[n,g] / smax[n]),
+ *             W_int8[n,k] = code[n,k] q[n,k/128]  (|W_int8| <= 127)
+ *   tokens    a = max_k |xr[m,k]|, xq = rne(xr 127/a), sx[m] = a/127
+ *   GEMM      acc[m,n] = sum_k xq[m,k] W_int8[n,k]   (exact int32)
+ *   epilogue  y[m,n] = (fl32(acc) * sw[n]) * sx[m],  sw[n] = smax[n]/127
+ *
+ * Conventions shared by every entry point:
+ *   - Every array pointer is a DEVICE pointer owned by the caller. The library
+ *     never allocates, frees or synchronises inside these calls (except
+ *     tl_get_status, which synchronises the given stream by design).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL means the
+ *     legacy default stream) and launches on the device current at the call.
+ *   - Arrays are row-major and densely packed. Every pointer must be 16-byte
+ *     aligned. Argument errors return before anything is launched.
+ *   - Shapes: K a positive multiple of 1024 and at most 32768; N a multiple of
+ *     128 (N = 0 or M = 0 is a valid empty call that launches nothing).
+ *   - Return value: a tl_status code. Errors found on the device (bounded waits
+ *     that gave up, codes outside {-1,0,1}) are recorded in a per-device status
+ *     word and reported by tl_get_status.
+ */
+#ifndef TL_H_
+#define TL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum tl_status {
+  TL_OK = 0,
+  TL_EINVAL = 1,        /* NULL pointer, negative size, misaligned pointer, bad dtype */
+  TL_EUNSUPPORTED = 2,  /* K not a multiple of 1024 or > 32768, N % 128, M > 32 on decode */
+  TL_ECUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+  TL_ETIMEOUT = 4,      /* a bounded device-side wait gave up (via tl_get_status) */
+  TL_EDATA = 5,         /* input data out of range, e.g. a code not in {-1,0,1} (via tl_get_status) */
+  TL_ENOSPACE = 6       /* a size exceeds the caller-provided capacity */
+};
+
+enum tl_dtype {
+  TL_I8 = 1,    /* int8 */
+  TL_F16 = 2,   /* IEEE binary16 */
+  TL_BF16 = 3,  /* bfloat16 */
+  TL_F32 = 4    /* IEEE binary32 */
+};
+
+/* Human-readable name of a tl_status value (static storage). */
+const char* tl_strerror(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int tl_version(void);
+
+/*
+ * Bytes of the three packed-weight arrays for an N x K layer:
+ *   packed  N * K / 4  (uint8; 2 bits per code)
+ *   qT      (K/128) * N (int8; q transposed, group-major)
+ *   sw      N * 4       (fp32)
+ * Any output pointer may be NULL. Errors: TL_EINVAL, TL_EUNSUPPORTED.
+ */
+int tl_packed_sizes(int N, int K, size_t* packed_bytes, size_t* qT_bytes, size_t* sw_bytes);
+
+/*
+ * Load-time weight packing (§4 "効いた高速化": the row-scale decomposition
+ * q = round(127 s / smax) and the 2-bit code representation of 前提).
+ *
+ *   codes   int8 [N, K], values in {-1, 0, +1}
+ *   s       fp16 bit patterns [N, K/128]; smax[n] = max_g |s[n,g]|
+ *   packed  out: uint32 words [N][K/16] (little endian). Word w of row n
+ *           covers k in [16w, 16w+16); the 2-bit field at bit 16h + 2j
+ *           holds e = code[n, 16w + 2j + h] + 1 (j = 0..7, h = 0, 1).
+ *   qT      out: int8 [K/128, N], qT[g,n] = rne(fl32(fl32(127 s[n,g]) / smax[n]))
+ *   sw      out: fp32 [N], sw[n] = fl32(smax[n] / 127); a row with smax = 0
+ *           gets q = 0 and sw = 0.
+ * A code outside {-1,0,1} records TL_EDATA in the device status word.
+ */
+int tl_pack_weights(const int8_t* codes, const uint16_t* s, int N, int K,
+                    uint8_t* packed, int8_t* qT, float* sw, void* stream);
+
+/*
+ * Input-side rotation fused with per-token int8 quantisation (前提: block
+ * Hadamard on the input side; §4: per-token int8 after the rotation).
+ *
+ *   x         bf16 bit patterns [M, K]
+ *   signs     optional int8 [K] of +1/-1 applied to x before the rotation
+ *             (NULL = all +1)
+ *   xq        out [M, K]: the int8 codes; xq_dtype = TL_I8 stores int8 (the
+ *             decode path's operand), TL_F16 stores the same integers as
+ *             exact fp16 values (the prefill path's tensor-core operand)
+ *   sx        out fp32 [M]
+ * Per token: xr = fl32 butterflies with strides 1,2,...,512 then x 1/32;
+ * a = max |xr|; inv = fl32(127/a); xq = clamp(rne(fl32(xr inv)), +-127);
+ * sx = fl32(a/127); a token with a = 0 gives xq = 0 and sx = 0.
+ */
+int tl_rotate_quant_act(const uint16_t* x, int M, int K, const int8_t* signs,
+                        void* xq, int xq_dtype, float* sx, void* stream);
+
+/*
+ * Workspace bytes that let tl_linear_prefill split the K dimension across
+ * CTAs when an M x N problem has too few output tiles to fill the GPU.
+ * With a smaller (or NULL) workspace the call still succeeds, unsplit.
+ */
+int tl_prefill_workspace_size(int M, int N, int K, size_t* bytes);
+
+/*
+ * Prefill (M >= 1) ternary linear layer on the tensor cores (§4: one int8
+ * GEMM plus per-row and per-token rescale; the expansion to W_int8 of §6's
+ * 31 ms is done inside the GEMM's main loop and never reaches memory).
+ *
+ *   packed, qT, sw   from tl_pack_weights
+ *   xq               fp16 [M, K] holding the int8 codes (tl_rotate_quant_act
+ *                    with TL_F16); sx fp32 [M]
+ *   y                out [M, N], y_dtype TL_BF16 (rne of the fp32 value) or TL_F32
+ *   acc_dbg          optional out int32 [M, N]: the exact integer accumulator
+ *   workspace        optional device scratch of ws_bytes (see
+ *                    tl_prefill_workspace_size); the call clears what it uses
+ * The integer accumulator is exact: the tensor cores take the int8 values as
+ * fp16 (exact), sum each 1024-column block in fp32 (every partial sum is an
+ * integer below 127*127*1024 < 2^24, hence exact) and the blocks are added in
+ * int32.
+ */
+int tl_linear_prefill(const uint8_t* packed, const int8_t* qT, const float* sw,
+                      const uint16_t* xq, const float* sx, int M, int N, int K,
+                      void* y, int y_dtype, int32_t* acc_dbg,
+                      void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Decode (1 <= M <= 32) ternary linear layer on the CUDA cores: streams the
+ * 2-bit weights once, decodes them in registers and takes int8 dot products
+ * (dp4a); same acc and y as tl_linear_prefill, bit for bit.
+ *
+ *   xq   int8 [M, K] (tl_rotate_quant_act with TL_I8); other arguments as
+ *        for tl_linear_prefill. M > 32 returns TL_EUNSUPPORTED.
+ */
+int tl_linear_decode(const uint8_t* packed, const int8_t* qT, const float* sw,
+                     const int8_t* xq, const float* sx, int M, int N, int K,
+                     void* y, int y_dtype, int32_t* acc_dbg, void* stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's status
+ * word: TL_OK, TL_ETIMEOUT or TL_EDATA (first error recorded), or TL_ECUDA if
+ * the synchronisation itself failed.
+ */
+int tl_get_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TL_H_ */

@@ -1,0 +1,156 @@
+// K1: input-side block Hadamard rotation fused with per-token int8 quantisation.
+//
+// Qiita item ecc183fae033565af7cb: 前提 (a block-wise Hadamard rotation on the
+// layer's input side), §1 "TP=2 への移植" (Sylvester structure, the last
+// butterfly stage combines the two 512-halves) and §4 "効いた高速化"
+// (activations quantised to int8 per token after the rotation).
+//
+// One CTA per token, one warp per 1024-column block. Lane l holds the 32
+// elements i = 256 j + 8 l + e (j = 0..3, e = 0..7), loaded as four
+// coalesced 16-byte vectors. Butterfly strides 1, 2, 4 act on e (registers),
+// 8..128 on the lane index (warp shuffles), 256 and 512 on j (registers), so
+// the stages run in the order 1, 2, 4, ..., 512 and every element sees the
+// same fp32 additions as a plain sequential FWHT.
+#include "tl_internal.cuh"
+
+#include <cuda_fp16.h>
+
+namespace tl {
+namespace {
+
+__device__ __forceinline__ void bfly(float& a, float& b) {
+  const float s = __fadd_rn(a, b);
+  const float d = __fsub_rn(a, b);
+  a = s;
+  b = d;
+}
+
+template <int XQ_DTYPE>
+__global__ void __launch_bounds__(1024)
+rotate_quant_kernel(const uint16_t* __restrict__ x, int K, const int8_t* __restrict__ signs,
+                    void* __restrict__ xq, float* __restrict__ sx) {
+  __shared__ float warp_max[32];
+  const int lane = threadIdx.x & 31;
+  const int blk = threadIdx.x >> 5;
+  const int nblk = blockDim.x >> 5;
+  const size_t m = blockIdx.x;
+  const size_t base = m * static_cast<size_t>(K) + static_cast<size_t>(blk) * kBlock;
+
+  float v[4][8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i0 = 256 * j + 8 * lane;
+    const uint4 raw = *reinterpret_cast<const uint4*>(x + base + i0);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t bits = (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+      v[j][e] = __uint_as_float(bits << 16);
+    }
+    if (signs != nullptr) {
+      const uint2 sraw = *reinterpret_cast<const uint2*>(signs + blk * kBlock + i0);
+      const uint32_t sw[2] = {sraw.x, sraw.y};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int8_t sg = static_cast<int8_t>((sw[e >> 2] >> (8 * (e & 3))) & 0xFFu);
+        if (sg < 0) v[j][e] = -v[j][e];
+      }
+    }
+  }
+
+  // strides 1, 2, 4: element bits 0..2
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if ((e & h) == 0) bfly(v[j][e], v[j][e + h]);
+      }
+    }
+  }
+  // strides 8, 16, 32, 64, 128: lane bits 0..4
+#pragma unroll
+  for (int t = 1; t < 32; t <<= 1) {
+    const bool upper = (lane & t) != 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float o = __shfl_xor_sync(0xffffffffu, v[j][e], t);
+        v[j][e] = upper ? __fsub_rn(o, v[j][e]) : __fadd_rn(v[j][e], o);
+      }
+    }
+  }
+  // strides 256, 512: j bits 0..1
+#pragma unroll
+  for (int h = 1; h < 4; h <<= 1) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if ((j & h) == 0) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) bfly(v[j][e], v[j + h][e]);
+      }
+    }
+  }
+
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      v[j][e] = __fmul_rn(v[j][e], 0.03125f);
+      amax = fmaxf(amax, fabsf(v[j][e]));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (lane == 0) warp_max[blk] = amax;
+  __syncthreads();
+  float a = 0.f;
+  for (int b = 0; b < nblk; ++b) a = fmaxf(a, warp_max[b]);
+
+  const float inv = a > 0.f ? __fdiv_rn(127.f, a) : 0.f;
+  if (threadIdx.x == 0) sx[m] = a > 0.f ? __fdiv_rn(a, 127.f) : 0.f;
+
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    int q[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      int t = __float2int_rn(__fmul_rn(v[j][e], inv));
+      q[e] = max(-127, min(127, t));
+    }
+    const size_t off = base + 256 * j + 8 * lane;
+    if (XQ_DTYPE == TL_I8) {
+      uint2 o;
+      o.x = (q[0] & 0xFF) | ((q[1] & 0xFF) << 8) | ((q[2] & 0xFF) << 16) | ((q[3] & 0xFF) << 24);
+      o.y = (q[4] & 0xFF) | ((q[5] & 0xFF) << 8) | ((q[6] & 0xFF) << 16) | ((q[7] & 0xFF) << 24);
+      *reinterpret_cast<uint2*>(static_cast<int8_t*>(xq) + off) = o;
+    } else {
+      uint32_t hw[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const uint32_t lo = __half_as_ushort(__int2half_rn(q[2 * p]));
+        const uint32_t hi = __half_as_ushort(__int2half_rn(q[2 * p + 1]));
+        hw[p] = lo | (hi << 16);
+      }
+      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(xq) + off) =
+          make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_rotate_quant(const uint16_t* x, int M, int K, const int8_t* signs, void* xq,
+                                int xq_dtype, float* sx, cudaStream_t st) {
+  const int threads = (K / kBlock) * 32;
+  if (xq_dtype == TL_I8)
+    rotate_quant_kernel<TL_I8><<<M, threads, 0, st>>>(x, K, signs, xq, sx);
+  else
+    rotate_quant_kernel<TL_F16><<<M, threads, 0, st>>>(x, K, signs, xq, sx);
+  return cudaGetLastError();
+}
+
+}  // namespace tl

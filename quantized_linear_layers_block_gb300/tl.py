@@ -1,0 +1,233 @@
+"""Python binding of the C ABI in include/tl.h (argument marshalling only).
+
+Every function here forwards device pointers, sizes and the current CUDA
+stream to libtl_gb300.so; all arithmetic of the layer runs in the library's
+CUDA kernels. PyTorch only allocates device memory and supplies the stream.
+If the library has not been built, loading it raises: there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtl_gb300.so")
+_lib = None
+_lock = threading.Lock()
+
+TL_OK, TL_EINVAL, TL_EUNSUPPORTED, TL_ECUDA, TL_ETIMEOUT, TL_EDATA, TL_ENOSPACE = range(7)
+TL_I8, TL_F16, TL_BF16, TL_F32 = 1, 2, 3, 4
+
+# name -> (restype, argtypes)
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+_PSZ = ctypes.POINTER(ctypes.c_size_t)
+SIGNATURES = {
+    "tl_strerror": (ctypes.c_char_p, [_I]),
+    "tl_version": (_I, []),
+    "tl_packed_sizes": (_I, [_I, _I, _PSZ, _PSZ, _PSZ]),
+    "tl_pack_weights": (_I, [_P, _P, _I, _I, _P, _P, _P, _P]),
+    "tl_rotate_quant_act": (_I, [_P, _I, _I, _P, _P, _I, _P, _P]),
+    "tl_prefill_workspace_size": (_I, [_I, _I, _I, _PSZ]),
+    "tl_linear_prefill": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P, _SZ, _P]),
+    "tl_linear_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P]),
+    "tl_get_status": (_I, [_P]),
+}
+
+
+class TLError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {tl_strerror(code)}")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it was never built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"{_LIB_PATH} is missing: build it with "
+                    "`python -m quantized_linear_layers_block_gb300.build` (needs nvcc)")
+            handle = ctypes.CDLL(_LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+    return _lib
+
+
+def tl_strerror(code: int) -> str:
+    return lib().tl_strerror(int(code)).decode()
+
+
+def _check(code: int, where: str) -> None:
+    if code != TL_OK:
+        raise TLError(code, where)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, torch.Tensor):
+        return t.data_ptr()
+    return int(t)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev_tensor(t: torch.Tensor, dtype: torch.dtype, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def tl_version() -> int:
+    return lib().tl_version()
+
+
+def tl_packed_sizes(N: int, K: int) -> tuple[int, int, int]:
+    a, b, c = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().tl_packed_sizes(N, K, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)), "tl_packed_sizes")
+    return a.value, b.value, c.value
+
+
+def tl_prefill_workspace_size(M: int, N: int, K: int) -> int:
+    b = ctypes.c_size_t()
+    _check(lib().tl_prefill_workspace_size(M, N, K, ctypes.byref(b)), "tl_prefill_workspace_size")
+    return b.value
+
+
+def tl_pack_weights(codes: torch.Tensor, s: torch.Tensor, stream=None):
+    """codes int8 [N,K] and s fp16 [N,K/128] (device) -> (packed uint8 [N,K/4], qT int8 [K/128,N], sw fp32 [N])."""
+    _dev_tensor(codes, torch.int8, "codes")
+    _dev_tensor(s, torch.float16, "s")
+    N, K = codes.shape
+    dev = codes.device
+    packed = torch.empty((N, K // 4), dtype=torch.uint8, device=dev)
+    qT = torch.empty((K // 128, N), dtype=torch.int8, device=dev)
+    sw = torch.empty((N,), dtype=torch.float32, device=dev)
+    _check(lib().tl_pack_weights(_ptr(codes), _ptr(s), N, K, _ptr(packed), _ptr(qT), _ptr(sw),
+                                 _stream(stream)), "tl_pack_weights")
+    return packed, qT, sw
+
+
+def tl_rotate_quant_act(x: torch.Tensor, signs: torch.Tensor | None = None, xq_dtype: int = TL_I8,
+                        xq: torch.Tensor | None = None, sx: torch.Tensor | None = None, stream=None):
+    """x bf16 [M,K] (device) -> (xq [M,K] int8 or fp16, sx fp32 [M])."""
+    _dev_tensor(x, torch.bfloat16, "x")
+    M, K = x.shape
+    tdt = torch.int8 if xq_dtype == TL_I8 else torch.float16
+    if xq is None:
+        xq = torch.empty((M, K), dtype=tdt, device=x.device)
+    if sx is None:
+        sx = torch.empty((M,), dtype=torch.float32, device=x.device)
+    if signs is not None:
+        _dev_tensor(signs, torch.int8, "signs")
+    _check(lib().tl_rotate_quant_act(_ptr(x), M, K, _ptr(signs), _ptr(xq), xq_dtype, _ptr(sx),
+                                     _stream(stream)), "tl_rotate_quant_act")
+    return xq, sx
+
+
+def _linear_out(M, N, y_dtype, dev, y):
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16 if y_dtype == TL_BF16 else torch.float32, device=dev)
+    return y
+
+
+def tl_linear_prefill(packed, qT, sw, xq, sx, N: int, K: int, y_dtype: int = TL_BF16,
+                      y: torch.Tensor | None = None, acc_dbg: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Tensor-core layer; xq is the fp16 image of the int8 codes [M,K]. Returns y [M,N]."""
+    _dev_tensor(xq, torch.float16, "xq")
+    M = xq.shape[0]
+    y = _linear_out(M, N, y_dtype, xq.device, y)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().tl_linear_prefill(_ptr(packed), _ptr(qT), _ptr(sw), _ptr(xq), _ptr(sx), M, N, K,
+                                   _ptr(y), y_dtype, _ptr(acc_dbg), _ptr(workspace), ws_bytes,
+                                   _stream(stream)), "tl_linear_prefill")
+    return y
+
+
+def tl_linear_decode(packed, qT, sw, xq, sx, N: int, K: int, y_dtype: int = TL_BF16,
+                     y: torch.Tensor | None = None, acc_dbg: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    """CUDA-core layer for M <= 32; xq int8 [M,K]. Returns y [M,N]."""
+    _dev_tensor(xq, torch.int8, "xq")
+    M = xq.shape[0]
+    y = _linear_out(M, N, y_dtype, xq.device, y)
+    _check(lib().tl_linear_decode(_ptr(packed), _ptr(qT), _ptr(sw), _ptr(xq), _ptr(sx), M, N, K,
+                                  _ptr(y), y_dtype, _ptr(acc_dbg), _stream(stream)), "tl_linear_decode")
+    return y
+
+
+def tl_get_status(stream=None) -> int:
+    return lib().tl_get_status(_stream(stream))
+
+
+class TernaryLinear:
+    """One ternary linear layer held in device memory (the library's public entry).
+
+    Built once from int8 codes [N,K] and fp16 group scales [N,K/128]; forward()
+    takes bf16 activations [M,K] on the host or the device and returns y [M,N]
+    where it found x. M <= 32 runs the decode kernel, larger M the tensor-core
+    prefill kernel; both give the same integer accumulator and the same y.
+    """
+
+    DECODE_MAX_M = 32
+
+    def __init__(self, codes: torch.Tensor, s: torch.Tensor, device="cuda", y_dtype: int = TL_BF16):
+        dev = torch.device(device)
+        codes = codes.to(dev, non_blocking=False).contiguous()
+        s = s.to(dev, non_blocking=False).contiguous()
+        self.N, self.K = codes.shape
+        self.device = dev
+        self.y_dtype = y_dtype
+        self.packed, self.qT, self.sw = tl_pack_weights(codes, s)
+        _check(tl_get_status(), "tl_pack_weights (device check)")
+        self._ws = None
+
+    def _workspace(self, M: int):
+        need = tl_prefill_workspace_size(M, self.N, self.K)
+        if need == 0:
+            return None
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty((need,), dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def forward(self, x: torch.Tensor, stream=None) -> torch.Tensor:
+        on_host = not x.is_cuda
+        xd = x.to(self.device, non_blocking=True) if on_host else x
+        M = xd.shape[0]
+        if M <= self.DECODE_MAX_M:
+            xq, sx = tl_rotate_quant_act(xd, xq_dtype=TL_I8, stream=stream)
+            y = tl_linear_decode(self.packed, self.qT, self.sw, xq, sx, self.N, self.K,
+                                 self.y_dtype, stream=stream)
+        else:
+            xq, sx = tl_rotate_quant_act(xd, xq_dtype=TL_F16, stream=stream)
+            y = tl_linear_prefill(self.packed, self.qT, self.sw, xq, sx, self.N, self.K,
+                                  self.y_dtype, workspace=self._workspace(M), stream=stream)
+        if on_host:
+            out = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+            out.copy_(y, non_blocking=True)
+            torch.cuda.current_stream(self.device).synchronize() if stream is None else stream.synchronize()
+            return out
+        return y
+
+    __call__ = forward
