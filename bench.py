@@ -1,0 +1,447 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 ternary linear layer (one JSON line on stdout).
+
+Metric: "ternary linear int8 TOPS @M=512; decode GEMV weight-stream GB/s @M=1".
+
+  prefill  (headline `value`): the fused gate+up projection of the 27B model,
+           M=512 tokens, K=5120, N=34816. One step = the 512-token batch through
+           64 layer buffers (64 distinct weight sets, 2.95 GB, so no step finds
+           its weights in the 129 MB L2): per layer rotate+quantise (K1) then the
+           tensor-core GEMM with fused rescale (K3). TOPS = 64 * 2 M N K / step.
+  decode   (`decode` object): M=1, K=5120, N=17408 over 64 layer buffers (1.47 GB);
+           per layer K1 then the CUDA-core GEMV (K2), captured in one CUDA graph
+           per step. GB/s = 64 * (packed + qT + sw bytes) / step.
+
+Inputs are seeded synthetic draws with the workloads' shapes and distributions,
+generated on the device; they are resident in HBM before timing starts.
+`e2e` repeats both through TernaryLinear.forward with pinned host buffers
+(host->device copy of x and device->host copy of y inside the timed region).
+`--impl reference` times the CPU oracle instead (see oracle/).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+LAYERS = 64
+PREFILL = dict(name="gate_up", M=512, K=5120, N=34816)
+DECODE = dict(name="decode", M=1, K=5120, N=17408)
+METRIC = "ternary linear int8 TOPS @M=512; decode GEMV weight-stream GB/s @M=1"
+CONFIG = {
+    "workload": "prefill fused gate+up M=512 K=5120 N=34816, one step = 64 layer buffers; "
+                "decode M=1 K=5120 N=17408, one step = 64 layer buffers",
+    "layers_per_step": LAYERS,
+    "l2": "inputs larger than L2: 64 distinct layer buffers (2.95 GB prefill, 1.47 GB decode weights)",
+}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def weight_bytes(N: int, K: int) -> int:
+    return N * K // 4 + (K // 128) * N + 4 * N
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.unlink(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [v for v in (num(r[1]) for r in rows) if v is not None]
+        mx = [v for v in (num(r[2]) for r in rows) if v is not None]
+        power = [v for v in (num(r[3]) for r in rows) if v is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def oracle_rate(kind: str, budget_s: float, min_reps: int = 1, M_s=None, N_s=None):
+    """Time the CPU oracle, as it stands, on a bounded sample of a workload.
+
+    Returns (rate, unit, sample description, reps, seconds, threads).
+    """
+    from oracle import ternary_linear as O
+    from quantized_linear_layers_block_gb300 import synth
+
+    cfg = PREFILL if kind == "prefill" else DECODE
+    M = M_s or cfg["M"]
+    N = N_s or (1024 if kind == "prefill" else cfg["N"])
+    L = synth.config_inputs(cfg["name"], M=M, N=N)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        O.layer(L.x_bits, L.codes, L.s)
+        reps += 1
+        el = time.perf_counter() - t0
+        if reps >= min_reps and el >= budget_s:
+            break
+    threads = os.cpu_count()
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        if info:
+            threads = max(i.get("num_threads", 1) for i in info)
+    except Exception:
+        pass
+    if kind == "prefill":
+        rate = 2.0 * M * N * cfg["K"] * reps / el / 1e12
+        unit = "TOPS"
+    else:
+        rate = weight_bytes(N, cfg["K"]) * reps / el / 1e9
+        unit = "GB/s"
+    sample = (f"oracle.layer (numpy; fp64 BLAS matmul on {threads} threads, the rest one thread) "
+              f"on M={M}, N={N} of {cfg['N']} rows, K={cfg['K']}: {reps} rep(s) in {el:.2f} s")
+    return rate, unit, sample, reps, el, threads
+
+
+def reference_main(args):
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return 0
+    steps = args.steps + args.warmup
+    per_step = max(0.02, min(1.0, 90.0 / max(steps, 1)))
+    # shrink the sample until one oracle step fits the per-step budget
+    M_s, N_s = PREFILL["M"], 1024
+    while True:
+        el = oracle_rate("prefill", 0.0, 1, M_s, N_s)[4]
+        if el <= per_step or (M_s <= 16 and N_s <= 128):
+            break
+        if N_s > 128:
+            N_s //= 2
+        else:
+            M_s //= 2
+    for _ in range(args.warmup):
+        oracle_rate("prefill", 0.0, 1, M_s, N_s)
+    rate, unit, sample, reps, el, threads = oracle_rate("prefill", 0.0, args.steps, M_s, N_s)
+    drate, dunit, dsample, _, _, _ = oracle_rate("decode", 0.0, 1, 1, 2048)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": unit, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / reps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+        "data": "synthetic", "config": dict(CONFIG, parallelism="cpu oracle"),
+        "cpu_baseline": {"value": rate, "unit": unit, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": rate, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "decode": {"metric": "decode GEMV weight-stream GB/s @M=1", "value": drate, "unit": dunit,
+                   "sample": dsample},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def main(argv=None):
+    global LAYERS
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-steps-per-step", type=int, default=32)
+    ap.add_argument("--layers", type=int, default=LAYERS,
+                    help="layer buffers per step (64 = the model's depth; fewer only for profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return reference_main(args)
+
+    import torch
+
+    LAYERS = args.layers
+    ws, rank, local = dist_info()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from quantized_linear_layers_block_gb300 import synth, tl
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+
+    def max_over_ranks(v: float) -> float:
+        if ws == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---------------- inputs: 64 layer buffers per workload, resident in HBM
+    P, D = PREFILL, DECODE
+    pre_layers, dec_layers = [], []
+    for li in range(LAYERS):
+        codes, s, x = synth.torch_config_layer(P["name"], li, device=str(dev))
+        lay = tl.TernaryLinear(codes, s, device=dev)
+        del codes, s
+        pre_layers.append((lay, x, torch.empty((P["M"], P["N"]), dtype=torch.bfloat16, device=dev)))
+        codes, s, x = synth.torch_config_layer(D["name"], li, device=str(dev))
+        lay = tl.TernaryLinear(codes, s, device=dev)
+        del codes, s
+        dec_layers.append((lay, x, torch.empty((D["M"], D["N"]), dtype=torch.bfloat16, device=dev)))
+    torch.cuda.synchronize()
+    if tl.tl_get_status() != tl.TL_OK:
+        raise RuntimeError("device status after packing")
+
+    xq_p = torch.empty((P["M"], P["K"]), dtype=torch.float16, device=dev)
+    sx_p = torch.empty((P["M"],), dtype=torch.float32, device=dev)
+    xq_d = torch.empty((D["M"], D["K"]), dtype=torch.int8, device=dev)
+    sx_d = torch.empty((D["M"],), dtype=torch.float32, device=dev)
+    ws_p = pre_layers[0][0]._workspace(P["M"])
+    stream = torch.cuda.current_stream(dev)
+
+    def prefill_layer(li, ev=None):
+        lay, x, y = pre_layers[li]
+        tl.tl_rotate_quant_act(x, xq_dtype=tl.TL_F16, xq=xq_p, sx=sx_p)
+        if ev is not None:
+            ev[0].record(stream)
+        tl.tl_linear_prefill(lay.packed, lay.qT, lay.sw, xq_p, sx_p, P["N"], P["K"], tl.TL_BF16,
+                             y=y, workspace=ws_p)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def decode_layer(li):
+        lay, x, y = dec_layers[li]
+        tl.tl_rotate_quant_act(x, xq_dtype=tl.TL_I8, xq=xq_d, sx=sx_d)
+        tl.tl_linear_decode(lay.packed, lay.qT, lay.sw, xq_d, sx_d, D["N"], D["K"], tl.TL_BF16, y=y)
+
+    def decode_kernel_only(li):
+        lay, _, y = dec_layers[li]
+        tl.tl_linear_decode(lay.packed, lay.qT, lay.sw, xq_d, sx_d, D["N"], D["K"], tl.TL_BF16, y=y)
+
+    # warm-up (also resolves driver entry points and kernel attributes before capture)
+    for _ in range(args.warmup):
+        for li in range(LAYERS):
+            prefill_layer(li)
+            decode_layer(li)
+    torch.cuda.synchronize()
+
+    g_dec = torch.cuda.CUDAGraph()
+    g_dk = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_dec, capture_error_mode="relaxed"):
+        for li in range(LAYERS):
+            decode_layer(li)
+    with torch.cuda.graph(g_dk, capture_error_mode="relaxed"):
+        for li in range(LAYERS):
+            decode_kernel_only(li)
+    for _ in range(args.warmup):
+        g_dec.replay()
+        g_dk.replay()
+    torch.cuda.synchronize()
+    if tl.tl_get_status() != tl.TL_OK:
+        raise RuntimeError("device status after warm-up")
+
+    uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    clocks = ClockSampler(uuid if uuid.startswith("GPU-") else f"GPU-{uuid}")
+    clocks.start()
+
+    # ---------------- timed prefill: K steps, each the batch through the layers
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K * LAYERS)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    i = 0
+    for _ in range(K):
+        for li in range(LAYERS):
+            prefill_layer(li, evs[i])
+            i += 1
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    pre_ms = max_over_ranks(t_start.elapsed_time(t_end))
+    k3_ms = statistics.fmean(a.elapsed_time(b) for a, b in evs)
+
+    # ---------------- timed decode: Kd steps (graph replays), each 1 token through the layers
+    Kd = K * args.decode_steps_per_step
+    barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for _ in range(Kd):
+        g_dec.replay()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    dec_ms = max_over_ranks(t_start.elapsed_time(t_end))
+    clk = clocks.stop()
+
+    # kernel-only decode time (graph of back-to-back K2 launches)
+    reps = max(8, Kd // 4)
+    t_start.record(stream)
+    for _ in range(reps):
+        g_dk.replay()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    k2_ms = t_start.elapsed_time(t_end) / (reps * LAYERS)
+    status = tl.tl_get_status()
+    if status != tl.TL_OK:
+        raise RuntimeError(f"device status after timing: {tl.tl_strerror(status)}")
+
+    # ---------------- end to end through TernaryLinear.forward with pinned host buffers
+    e2e_steps = 0 if args.no_e2e else max(1, min(K, 8))
+    e2e_dsteps = 0 if args.no_e2e else max(1, min(Kd, 64))
+    xh_p = [x.cpu().pin_memory() for _, x, _ in pre_layers]
+    xh_d = [x.cpu().pin_memory() for _, x, _ in dec_layers]
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for li in range(LAYERS):
+            pre_layers[li][0].forward(xh_p[li])
+    e2e_pre_s = max(max_over_ranks(time.perf_counter() - t0), 1e-9)
+    t0 = time.perf_counter()
+    for _ in range(e2e_dsteps):
+        for li in range(LAYERS):
+            dec_layers[li][0].forward(xh_d[li])
+    e2e_dec_s = max(max_over_ranks(time.perf_counter() - t0), 1e-9)
+
+    # ---------------- figures
+    flop_layer = 2.0 * P["M"] * P["N"] * P["K"]
+    tops = ws * K * LAYERS * flop_layer / (pre_ms * 1e-3) / 1e12
+    wb = weight_bytes(D["N"], D["K"])
+    gbs = ws * Kd * LAYERS * wb / (dec_ms * 1e-3) / 1e9
+    peaks, peak_src = load_peaks()
+    tc_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    k3_tops = flop_layer / (k3_ms * 1e-3) / 1e12
+    dec_alg_bytes = wb + D["M"] * D["K"] + 4 * D["M"] + 2 * D["M"] * D["N"]
+    k2_gbs = dec_alg_bytes / (k2_ms * 1e-3) / 1e9
+    traffic = _profiled_traffic()
+
+    line = {
+        "metric": METRIC, "value": tops, "unit": "TOPS", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": pre_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": dict(CONFIG, layers_per_step=LAYERS, parallelism=f"replicas x{ws}"),
+        "roofline": {"bound": "tensor", "achieved": k3_tops, "peak": tc_peak, "unit": "TFLOP/s",
+                     "frac": k3_tops / tc_peak, "traffic": traffic.get("prefill_kernel"),
+                     "kernel": "prefill_kernel (K3)",
+                     "peak_source": f"{peak_src} bf16_tflops_sustained (the int8 GEMM runs on "
+                                    "kind::f16 tensor cores; fp16 and bf16 share the rate)"},
+        "decode": {
+            "metric": "decode GEMV weight-stream GB/s @M=1", "value": gbs, "unit": "GB/s",
+            "steps": Kd, "ms_per_step": dec_ms / Kd, "kernel_us": k2_ms * 1e3,
+            "roofline": {"bound": "hbm", "achieved": k2_gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": k2_gbs / hbm_peak, "traffic": traffic.get("decode_kernel"),
+                         "kernel": "decode kernel M=1 (K2), graph of back-to-back launches",
+                         "peak_source": f"{peak_src} hbm_gbs"},
+            "e2e": {"value": ws * e2e_dsteps * LAYERS * wb / e2e_dec_s / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": LAYERS * D["M"] * D["K"] * 2,
+                    "d2h_bytes_per_step": LAYERS * D["M"] * D["N"] * 2},
+        },
+        "kernels_us": {"prefill_kernel": k3_ms * 1e3, "decode_kernel": k2_ms * 1e3,
+                       "prefill_step_rest": (pre_ms / (K * LAYERS) - k3_ms) * 1e3},
+        "e2e": {"value": ws * e2e_steps * LAYERS * flop_layer / e2e_pre_s / 1e12, "unit": "TOPS",
+                "h2d_bytes_per_step": LAYERS * P["M"] * P["K"] * 2,
+                "d2h_bytes_per_step": LAYERS * P["M"] * P["N"] * 2},
+        "gpu_launches": K * LAYERS * 2 + Kd * LAYERS * 2,
+        "clocks": clk,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        rate, unit, sample, _, _, threads = oracle_rate("prefill", 10.0)
+        line["cpu_baseline"] = {"value": rate, "unit": unit, "cores": threads, "kind": "oracle",
+                                "sample": sample}
+        drate, dunit, dsample, _, _, _ = oracle_rate("decode", 5.0)
+        line["decode"]["cpu_baseline"] = {"value": drate, "unit": dunit, "cores": threads,
+                                          "kind": "oracle", "sample": dsample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def _profiled_traffic() -> dict:
+    """DRAM bytes per launch of the current kernels from the committed ncu summary, if any."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -163,3 +163,48 @@ def config_inputs(name: str, layer: int = 0, M: int | None = None, N: int | None
     if c["M"] is None:
         raise ValueError("sweep configs need an explicit M")
     return make_layer(config_seed(name, layer), **c)
+
+
+# --------------------------------------------------------------------------
+# Device-side generation of many layers for benchmarking (same recipe, drawn
+# with torch's CUDA generator so that 64 layer buffers take seconds, not
+# minutes). Parity tests use the numpy generator above.
+# --------------------------------------------------------------------------
+
+def torch_layer(seed: int, M: int, K: int, N: int, *, p0: float, mu: float, sigma: float,
+                x_kind: str, n_outliers: int = 0, outlier_factor: float = 1.0,
+                device: str = "cuda"):
+    """(codes int8 [N,K], s fp16 [N,K/128], x bf16 [M,K]) on `device`, seeded."""
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    codes = torch.empty((N, K), dtype=torch.int8, device=device)
+    rows = max(1, (1 << 26) // K)
+    for r0 in range(0, N, rows):
+        r1 = min(N, r0 + rows)
+        u = torch.rand((r1 - r0, K), generator=g, device=device)
+        c = torch.where(u < p0, 0, torch.where(u < p0 + (1.0 - p0) * 0.5, 1, -1))
+        codes[r0:r1] = c.to(torch.int8)
+    s = torch.exp(torch.randn((N, K // 128), generator=g, device=device) * sigma + mu).to(torch.float16)
+    if x_kind == "gauss":
+        x = torch.randn((M, K), generator=g, device=device)
+        if n_outliers > 0:
+            ch = torch.randperm(K, generator=g, device=device)[:n_outliers]
+            x[:, ch] *= outlier_factor
+    elif x_kind == "t3":
+        z = torch.randn((M, K), generator=g, device=device)
+        chi2 = (torch.randn((3, M, K), generator=g, device=device) ** 2).sum(0)
+        x = z / torch.sqrt(chi2 / 3.0)
+    else:
+        raise ValueError(x_kind)
+    return codes, s, x.to(torch.bfloat16)
+
+
+def torch_config_layer(name: str, layer: int, M: int | None = None, device: str = "cuda"):
+    """A named workload's layer drawn on the device (see torch_layer)."""
+    c = dict(CONFIGS[name])
+    c.pop("cfg")
+    if M is not None:
+        c["M"] = M
+    return torch_layer(config_seed(name, layer), device=device, **c)
