@@ -5,15 +5,20 @@
 // is the idea of §5 "効かなかったもの" (a dp4a decode GEMV), here computing
 // exactly the quantised layer so that decode and prefill agree bit for bit.
 //
-// Each CTA owns 32 consecutive output rows. The activations of all tokens
-// for a slab of K are staged in shared memory once, permuted so that a
-// 32-bit word of packed codes shifted by 2t and masked with 0x03030303 lines
-// up byte for byte with activation word t:
+// Each CTA owns 32 consecutive output rows, 4 per warp. Its first weight
+// loads are issued at entry, before the kernel waits (programmatic dependent
+// launch) for the activations of the preceding kernel, so the 2-bit weight
+// stream of one layer overlaps the tail of the previous one. The packed
+// weights, qT and sw are therefore read before that wait: they must be
+// complete when the kernel is launched (tl_pack_weights at load time).
+// The activations are staged in shared memory, permuted so that a 32-bit word
+// of packed codes shifted by 2t and masked with 0x03030303 lines up byte for
+// byte with activation word t:
 //   e-bytes of (w >> 2t) & 0x03030303  ->  k = 2t, 2t+8, 2t+1, 2t+9
 // dp4a(e, x) then gives sum (code + 1) x; the per-chunk activation sum is
 // subtracted and the result multiplied by q[n, g] (integer, exact).
-// Lane l of a warp always owns the 32-code chunks l, l+32, ... of a row, so
-// a warp-wide load of one row is fully coalesced 8-byte accesses.
+// Lane l of a warp owns the 32-code chunks l, l+32, ... of a row, so a
+// warp-wide load of one row is fully coalesced 8-byte accesses.
 #include "tl_internal.cuh"
 
 #include <cuda_bf16.h>
@@ -23,8 +28,8 @@ namespace {
 
 constexpr int kDecWarps = 8;
 constexpr int kRowsPerCta = 32;
+constexpr int kRowsPerWarp = kRowsPerCta / kDecWarps;
 constexpr int kQStride = kRowsPerCta + 4;   // padded: conflict-free q reads
-constexpr int kLoadBatch = 8;               // chunk loads in flight per lane
 constexpr size_t kSlabBudget = 96 * 1024;
 
 __host__ __device__ constexpr int slab_k(int mt, int K) {
@@ -43,15 +48,139 @@ __device__ __forceinline__ void store_y(void* y, int y_dtype, size_t idx, float 
     static_cast<__nv_bfloat16*>(y)[idx] = __float2bfloat16_rn(v);
 }
 
+// Permute 32 activation bytes (one chunk) into dp4a order; returns their sum.
+__device__ __forceinline__ int permute_chunk(uint4 u0, uint4 u1, uint4& p0, uint4& p1) {
+  p0.x = __byte_perm(u0.x, u0.z, 0x5140);
+  p0.y = __byte_perm(u0.x, u0.z, 0x7362);
+  p0.z = __byte_perm(u0.y, u0.w, 0x5140);
+  p0.w = __byte_perm(u0.y, u0.w, 0x7362);
+  p1.x = __byte_perm(u1.x, u1.z, 0x5140);
+  p1.y = __byte_perm(u1.x, u1.z, 0x7362);
+  p1.z = __byte_perm(u1.y, u1.w, 0x5140);
+  p1.w = __byte_perm(u1.y, u1.w, 0x7362);
+  int s = __dp4a(static_cast<int>(u0.x), 0x01010101, 0);
+  s = __dp4a(static_cast<int>(u0.y), 0x01010101, s);
+  s = __dp4a(static_cast<int>(u0.z), 0x01010101, s);
+  s = __dp4a(static_cast<int>(u0.w), 0x01010101, s);
+  s = __dp4a(static_cast<int>(u1.x), 0x01010101, s);
+  s = __dp4a(static_cast<int>(u1.y), 0x01010101, s);
+  s = __dp4a(static_cast<int>(u1.z), 0x01010101, s);
+  s = __dp4a(static_cast<int>(u1.w), 0x01010101, s);
+  return s;
+}
+
+// sum_k (code_k + 1) x_k over one 32-code chunk, starting from t.
+__device__ __forceinline__ int dot_chunk(uint32_t wa, uint32_t wb, uint4 xa, uint4 xb, int t) {
+  t = __dp4a(static_cast<int>(wa & 0x03030303u), static_cast<int>(xa.x), t);
+  t = __dp4a(static_cast<int>((wa >> 2) & 0x03030303u), static_cast<int>(xa.y), t);
+  t = __dp4a(static_cast<int>((wa >> 4) & 0x03030303u), static_cast<int>(xa.z), t);
+  t = __dp4a(static_cast<int>((wa >> 6) & 0x03030303u), static_cast<int>(xa.w), t);
+  t = __dp4a(static_cast<int>(wb & 0x03030303u), static_cast<int>(xb.x), t);
+  t = __dp4a(static_cast<int>((wb >> 2) & 0x03030303u), static_cast<int>(xb.y), t);
+  t = __dp4a(static_cast<int>((wb >> 4) & 0x03030303u), static_cast<int>(xb.z), t);
+  t = __dp4a(static_cast<int>((wb >> 6) & 0x03030303u), static_cast<int>(xb.w), t);
+  return t;
+}
+
+// q of this CTA's rows for all groups (qT is group-major: 32 contiguous bytes per group).
+__device__ __forceinline__ void stage_q(const int8_t* __restrict__ qT, int N, int G, int n0,
+                                        int8_t* qs) {
+  for (int i = threadIdx.x; i < G * (kRowsPerCta / 4); i += blockDim.x) {
+    const int g = i / (kRowsPerCta / 4), r4 = i % (kRowsPerCta / 4);
+    *reinterpret_cast<uint32_t*>(qs + g * kQStride + 4 * r4) =
+        *reinterpret_cast<const uint32_t*>(qT + static_cast<size_t>(g) * N + n0 + 4 * r4);
+  }
+}
+
+// ---------------------------------------------------------------- M = 1
+// PL chunks of 32 codes per lane and row (K = 1024 PL). Fully unrolled over
+// the warp's 4 rows and the PL chunks, so every ring slot is a register; RR
+// rows of weights are in flight per warp. The activations are staged once per
+// CTA as two half-chunk arrays (conflict-free 16-byte reads) with their sums.
+template <int PL>
+__global__ void __launch_bounds__(kDecWarps * 32)
+decode1_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ qT,
+               const float* __restrict__ sw, const int8_t* __restrict__ xq,
+               const float* __restrict__ sx, int N, void* __restrict__ y, int y_dtype,
+               int32_t* __restrict__ acc_dbg) {
+  constexpr int K = PL * kBlock;
+  constexpr int G = K / kGroup;
+  constexpr int NC = K / 32;                           // chunks per row
+  constexpr int RR = PL <= 4 ? 4 : (PL <= 8 ? 2 : 1);  // rows of weights in flight per warp
+  __shared__ __align__(16) uint4 xw0[NC];
+  __shared__ __align__(16) uint4 xw1[NC];
+  __shared__ int csum[NC];
+  __shared__ __align__(16) int8_t qs[G * kQStride];
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int n0 = blockIdx.x * kRowsPerCta;
+  const uint2* pw = reinterpret_cast<const uint2*>(packed) + static_cast<size_t>(n0 + warp) * NC + lane;
+  constexpr size_t kRowStep = static_cast<size_t>(kDecWarps) * NC;   // uint2 between a warp's rows
+
+  uint2 ring[RR][PL];
+#pragma unroll
+  for (int j = 0; j < RR; ++j) {
+#pragma unroll
+    for (int i = 0; i < PL; ++i) ring[j][i] = __ldg(pw + j * kRowStep + i * 32);
+  }
+  pdl_launch_dependents();
+  stage_q(qT, N, G, n0, qs);
+  pdl_wait_prior();
+  for (int c = tid; c < NC; c += blockDim.x) {
+    const uint4* src = reinterpret_cast<const uint4*>(xq + 32 * c);
+    uint4 p0, p1;
+    csum[c] = permute_chunk(src[0], src[1], p0, p1);
+    xw0[c] = p0;
+    xw1[c] = p1;
+  }
+  __syncthreads();
+  const float sx0 = sx[0];
+
+#pragma unroll
+  for (int j = 0; j < kRowsPerWarp; ++j) {
+    const int r = warp + kDecWarps * j;
+    int acc = 0;
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+      const int c = i * 32 + lane;
+      const uint2 wv = ring[j % RR][i];
+      if (j + RR < kRowsPerWarp) ring[j % RR][i] = __ldg(pw + (j + RR) * kRowStep + i * 32);
+      const int t = dot_chunk(wv.x, wv.y, xw0[c], xw1[c], -csum[c]);
+      acc += static_cast<int>(qs[(8 * i + (lane >> 2)) * kQStride + r]) * t;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+      const int n = n0 + r;
+      if (acc_dbg != nullptr) acc_dbg[n] = acc;
+      store_y(y, y_dtype, n, __fmul_rn(__fmul_rn(__int2float_rn(acc), sw[n]), sx0));
+    }
+  }
+}
+
+// ---------------------------------------------------------------- 1 <= M <= 32
+// MT tokens per pass (M rounded up to a power of two). A warp walks its
+// (row, chunk) items in order and keeps PF weight loads in flight; the first
+// PF are issued at entry. When MT * K does not fit in shared memory, K is
+// processed in slabs and per-row partial sums are kept in shared memory.
+template <int MT>
+struct DecodeTraits {
+  static constexpr int PF = MT <= 2 ? 16 : 8;
+};
+
 template <int MT>
 __global__ void __launch_bounds__(kDecWarps * 32)
 decode_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ qT,
               const float* __restrict__ sw, const int8_t* __restrict__ xq,
               const float* __restrict__ sx, int M, int N, int K, int KS, void* __restrict__ y,
               int y_dtype, int32_t* __restrict__ acc_dbg) {
+  constexpr int PF = DecodeTraits<MT>::PF;
   extern __shared__ __align__(16) uint8_t smem[];
   const int G = K / kGroup;
-  uint32_t* xw = reinterpret_cast<uint32_t*>(smem);                         // [MT][KS/4]
+  uint4* xw0 = reinterpret_cast<uint4*>(smem);                                    // [MT][KS/32]
+  uint4* xw1 = reinterpret_cast<uint4*>(smem + static_cast<size_t>(MT) * KS / 2);  // [MT][KS/32]
   int32_t* csum = reinterpret_cast<int32_t*>(smem + static_cast<size_t>(MT) * KS);  // [MT][KS/32]
   int8_t* qs = reinterpret_cast<int8_t*>(smem + static_cast<size_t>(MT) * KS * 9 / 8);  // [G][kQStride]
   int32_t* part = reinterpret_cast<int32_t*>(
@@ -61,123 +190,118 @@ decode_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ qT
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int n0 = blockIdx.x * kRowsPerCta;
-
-  // q of this CTA's rows, all groups (qT is group-major: 32 contiguous bytes per group).
-  for (int i = tid; i < G * (kRowsPerCta / 4); i += blockDim.x) {
-    const int g = i / (kRowsPerCta / 4), r4 = i % (kRowsPerCta / 4);
-    const uint32_t v =
-        *reinterpret_cast<const uint32_t*>(qT + static_cast<size_t>(g) * N + n0 + 4 * r4);
-    *reinterpret_cast<uint32_t*>(qs + g * kQStride + 4 * r4) = v;
-  }
-
   const int nslab = (K + KS - 1) / KS;
+  const size_t row_step = static_cast<size_t>(kDecWarps) * (K / 32);   // uint2 between a warp's rows
+  const uint2* prow0 = reinterpret_cast<const uint2*>(packed) + static_cast<size_t>(n0 + warp) * (K / 32) + lane;
+
+  uint2 ring[PF];
+  int per_lane = min(KS, K) / kBlock;
+  int items = kRowsPerWarp * per_lane;
+  // position of the next item to load (row slot, chunk)
+  int prr = 0, pci = 0;
+#pragma unroll
+  for (int u = 0; u < PF; ++u) {
+    if (u < items) {
+      ring[u] = __ldg(prow0 + prr * row_step + pci * 32);
+      if (++pci == per_lane) {
+        pci = 0;
+        ++prr;
+      }
+    }
+  }
+  pdl_launch_dependents();
+  stage_q(qT, N, G, n0, qs);
+  pdl_wait_prior();
+
   for (int sl = 0; sl < nslab; ++sl) {
     const int k0 = sl * KS;
     const int ks = min(KS, K - k0);
     const int nchunk = ks / 32;
-    __syncthreads();  // previous slab fully consumed
-    // Stage activations: one 32-code chunk per thread iteration.
+    per_lane = nchunk / 32;  // ks is a multiple of 1024
+    items = kRowsPerWarp * per_lane;
+    const uint2* prow = prow0 + k0 / 32;
+    if (sl > 0) {
+      __syncthreads();  // previous slab fully consumed
+      prr = 0;
+      pci = 0;
+#pragma unroll
+      for (int u = 0; u < PF; ++u) {
+        if (u < items) {
+          ring[u] = __ldg(prow + prr * row_step + pci * 32);
+          if (++pci == per_lane) {
+            pci = 0;
+            ++prr;
+          }
+        }
+      }
+    }
     for (int i = tid; i < MT * nchunk; i += blockDim.x) {
       const int m = i / nchunk, c = i % nchunk;
       uint4 u0 = make_uint4(0, 0, 0, 0), u1 = u0;
       if (m < M) {
-        const uint4* src =
-            reinterpret_cast<const uint4*>(xq + static_cast<size_t>(m) * K + k0 + 32 * c);
+        const uint4* src = reinterpret_cast<const uint4*>(xq + static_cast<size_t>(m) * K + k0 + 32 * c);
         u0 = src[0];
         u1 = src[1];
       }
       uint4 p0, p1;
-      p0.x = __byte_perm(u0.x, u0.z, 0x5140);
-      p0.y = __byte_perm(u0.x, u0.z, 0x7362);
-      p0.z = __byte_perm(u0.y, u0.w, 0x5140);
-      p0.w = __byte_perm(u0.y, u0.w, 0x7362);
-      p1.x = __byte_perm(u1.x, u1.z, 0x5140);
-      p1.y = __byte_perm(u1.x, u1.z, 0x7362);
-      p1.z = __byte_perm(u1.y, u1.w, 0x5140);
-      p1.w = __byte_perm(u1.y, u1.w, 0x7362);
-      uint4* dst = reinterpret_cast<uint4*>(xw + static_cast<size_t>(m) * (KS / 4) + 8 * c);
-      dst[0] = p0;
-      dst[1] = p1;
-      int s = 0;
-      s = __dp4a(static_cast<int>(u0.x), 0x01010101, s);
-      s = __dp4a(static_cast<int>(u0.y), 0x01010101, s);
-      s = __dp4a(static_cast<int>(u0.z), 0x01010101, s);
-      s = __dp4a(static_cast<int>(u0.w), 0x01010101, s);
-      s = __dp4a(static_cast<int>(u1.x), 0x01010101, s);
-      s = __dp4a(static_cast<int>(u1.y), 0x01010101, s);
-      s = __dp4a(static_cast<int>(u1.z), 0x01010101, s);
-      s = __dp4a(static_cast<int>(u1.w), 0x01010101, s);
-      csum[m * (KS / 32) + c] = s;
+      csum[m * (KS / 32) + c] = permute_chunk(u0, u1, p0, p1);
+      xw0[m * (KS / 32) + c] = p0;
+      xw1[m * (KS / 32) + c] = p1;
     }
     __syncthreads();
 
-    const int per_lane = nchunk / 32;  // ks is a multiple of 1024
-    for (int r = warp; r < kRowsPerCta; r += kDecWarps) {
-      const int n = n0 + r;
-      const uint2* prow = reinterpret_cast<const uint2*>(packed + static_cast<size_t>(n) * (K / 16)) + k0 / 32;
-      int acc[MT];
+    int acc[MT];
 #pragma unroll
-      for (int m = 0; m < MT; ++m) acc[m] = 0;
-
-      for (int cb = 0; cb < per_lane; cb += kLoadBatch) {
-        uint2 wv[kLoadBatch];
+    for (int m = 0; m < MT; ++m) acc[m] = 0;
+    int rr = 0, ci = 0;   // row slot and chunk of the item being consumed
+    for (int jb = 0; jb < items; jb += PF) {
 #pragma unroll
-        for (int b = 0; b < kLoadBatch; ++b) {
-          if (cb + b < per_lane) wv[b] = __ldg(prow + (cb + b) * 32 + lane);
-        }
-#pragma unroll
-        for (int b = 0; b < kLoadBatch; ++b) {
-          if (cb + b < per_lane) {
-            const int c = (cb + b) * 32 + lane;          // chunk index within the slab
-            const int g = (k0 + 32 * c) / kGroup;
-            const int q = qs[g * kQStride + r];
-            const int hsel = (c >> 2) & 1;                 // alternate halves: no bank conflicts
-            const uint32_t wa = hsel ? wv[b].y : wv[b].x;
-            const uint32_t wb = hsel ? wv[b].x : wv[b].y;
-            int ea[4], eb[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              ea[t] = static_cast<int>((wa >> (2 * t)) & 0x03030303u);
-              eb[t] = static_cast<int>((wb >> (2 * t)) & 0x03030303u);
-            }
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-              const uint32_t* xm = xw + static_cast<size_t>(m) * (KS / 4) + 8 * c;
-              const uint4 xa = *reinterpret_cast<const uint4*>(xm + 4 * hsel);
-              const uint4 xb = *reinterpret_cast<const uint4*>(xm + 4 * (hsel ^ 1));
-              int t = -csum[m * (KS / 32) + c];
-              t = __dp4a(ea[0], static_cast<int>(xa.x), t);
-              t = __dp4a(ea[1], static_cast<int>(xa.y), t);
-              t = __dp4a(ea[2], static_cast<int>(xa.z), t);
-              t = __dp4a(ea[3], static_cast<int>(xa.w), t);
-              t = __dp4a(eb[0], static_cast<int>(xb.x), t);
-              t = __dp4a(eb[1], static_cast<int>(xb.y), t);
-              t = __dp4a(eb[2], static_cast<int>(xb.z), t);
-              t = __dp4a(eb[3], static_cast<int>(xb.w), t);
-              acc[m] += q * t;
+      for (int u = 0; u < PF; ++u) {
+        if (jb + u < items) {
+          const uint2 wv = ring[u];
+          if (jb + u + PF < items) {
+            ring[u] = __ldg(prow + prr * row_step + pci * 32);
+            if (++pci == per_lane) {
+              pci = 0;
+              ++prr;
             }
           }
-        }
-      }
+          const int r = warp + kDecWarps * rr;
+          const int c = ci * 32 + lane;                  // chunk index within the slab
+          const int q = qs[((k0 / kGroup) + (c >> 2)) * kQStride + r];
 #pragma unroll
-      for (int m = 0; m < MT; ++m) {
+          for (int m = 0; m < MT; ++m) {
+            const int t = dot_chunk(wv.x, wv.y, xw0[m * (KS / 32) + c], xw1[m * (KS / 32) + c],
+                                    -csum[m * (KS / 32) + c]);
+            acc[m] += q * t;
+          }
+          if (++ci == per_lane) {
+            // row r of this slab is complete: reduce over the warp
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
-      }
-      // every lane now holds all MT totals; lane m owns token m
-      int mine = 0;
+            for (int m = 0; m < MT; ++m) {
 #pragma unroll
-      for (int m = 0; m < MT; ++m)
-        if (lane == m) mine = acc[m];
-      if (lane < MT) {
-        if (sl > 0) mine += part[r * MT + lane];
-        if (sl + 1 < nslab) {
-          part[r * MT + lane] = mine;
-        } else if (lane < M) {
-          const size_t idx = static_cast<size_t>(lane) * N + n;
-          if (acc_dbg != nullptr) acc_dbg[idx] = mine;
-          const float v = __fmul_rn(__fmul_rn(__int2float_rn(mine), sw[n]), sx[lane]);
-          store_y(y, y_dtype, idx, v);
+              for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
+            }
+            int mine = 0;
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+              if (lane == m) mine = acc[m];
+            if (lane < MT) {
+              if (sl > 0) mine += part[r * MT + lane];
+              if (sl + 1 < nslab) {
+                part[r * MT + lane] = mine;
+              } else if (lane < M) {
+                const int n = n0 + r;
+                const size_t idx = static_cast<size_t>(lane) * N + n;
+                if (acc_dbg != nullptr) acc_dbg[idx] = mine;
+                store_y(y, y_dtype, idx, __fmul_rn(__fmul_rn(__int2float_rn(mine), sw[n]), sx[lane]));
+              }
+            }
+#pragma unroll
+            for (int m = 0; m < MT; ++m) acc[m] = 0;
+            ci = 0;
+            ++rr;
+          }
         }
       }
     }
@@ -196,10 +320,16 @@ cudaError_t launch_mt(const uint32_t* packed, const int8_t* qT, const float* sw,
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int blocks = N / kRowsPerCta;
-  decode_kernel<MT><<<blocks, kDecWarps * 32, smem, st>>>(packed, qT, sw, xq, sx, M, N, K, KS, y,
-                                                          y_dtype, acc_dbg);
-  return cudaGetLastError();
+  return launch_pdl(decode_kernel<MT>, dim3(N / kRowsPerCta), dim3(kDecWarps * 32), smem, st,
+                    packed, qT, sw, xq, sx, M, N, K, KS, y, y_dtype, acc_dbg);
+}
+
+template <int PL>
+cudaError_t launch_m1(const uint32_t* packed, const int8_t* qT, const float* sw, const int8_t* xq,
+                      const float* sx, int N, void* y, int y_dtype, int32_t* acc_dbg,
+                      cudaStream_t st) {
+  return launch_pdl(decode1_kernel<PL>, dim3(N / kRowsPerCta), dim3(kDecWarps * 32), 0, st,
+                    packed, qT, sw, xq, sx, N, y, y_dtype, acc_dbg);
 }
 
 }  // namespace
@@ -207,6 +337,19 @@ cudaError_t launch_mt(const uint32_t* packed, const int8_t* qT, const float* sw,
 cudaError_t launch_decode(const uint32_t* packed, const int8_t* qT, const float* sw,
                           const int8_t* xq, const float* sx, int M, int N, int K, void* y,
                           int y_dtype, int32_t* acc_dbg, cudaStream_t st) {
+  if (M == 1) {
+    switch (K / kBlock) {
+      case 1: return launch_m1<1>(packed, qT, sw, xq, sx, N, y, y_dtype, acc_dbg, st);
+      case 2: return launch_m1<2>(packed, qT, sw, xq, sx, N, y, y_dtype, acc_dbg, st);
+      case 3: return launch_m1<3>(packed, qT, sw, xq, sx, N, y, y_dtype, acc_dbg, st);
+      case 4: return launch_m1<4>(packed, qT, sw, xq, sx, N, y, y_dtype, acc_dbg, st);
+      case 5: return launch_m1<5>(packed, qT, sw, xq, sx, N, y, y_dtype, acc_dbg, st);
+      case 8: return launch_m1<8>(packed, qT, sw, xq, sx, N, y, y_dtype, acc_dbg, st);
+      case 16: return launch_m1<16>(packed, qT, sw, xq, sx, N, y, y_dtype, acc_dbg, st);
+      case 17: return launch_m1<17>(packed, qT, sw, xq, sx, N, y, y_dtype, acc_dbg, st);
+      default: break;
+    }
+  }
   if (M <= 1) return launch_mt<1>(packed, qT, sw, xq, sx, M, N, K, y, y_dtype, acc_dbg, st);
   if (M <= 2) return launch_mt<2>(packed, qT, sw, xq, sx, M, N, K, y, y_dtype, acc_dbg, st);
   if (M <= 4) return launch_mt<4>(packed, qT, sw, xq, sx, M, N, K, y, y_dtype, acc_dbg, st);

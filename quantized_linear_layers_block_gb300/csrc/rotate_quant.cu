@@ -35,6 +35,10 @@ rotate_quant_kernel(const uint16_t* __restrict__ x, int K, const int8_t* __restr
   const int nblk = blockDim.x >> 5;
   const size_t m = blockIdx.x;
   const size_t base = m * static_cast<size_t>(K) + static_cast<size_t>(blk) * kBlock;
+  // x may be the output of the preceding kernel; once it is complete, the next
+  // kernel (the layer's GEMM) may start its weight-only prologue.
+  pdl_wait_prior();
+  pdl_launch_dependents();
 
   float v[4][8];
 #pragma unroll
@@ -147,10 +151,8 @@ cudaError_t launch_rotate_quant(const uint16_t* x, int M, int K, const int8_t* s
                                 int xq_dtype, float* sx, cudaStream_t st) {
   const int threads = (K / kBlock) * 32;
   if (xq_dtype == TL_I8)
-    rotate_quant_kernel<TL_I8><<<M, threads, 0, st>>>(x, K, signs, xq, sx);
-  else
-    rotate_quant_kernel<TL_F16><<<M, threads, 0, st>>>(x, K, signs, xq, sx);
-  return cudaGetLastError();
+    return launch_pdl(rotate_quant_kernel<TL_I8>, dim3(M), dim3(threads), 0, st, x, K, signs, xq, sx);
+  return launch_pdl(rotate_quant_kernel<TL_F16>, dim3(M), dim3(threads), 0, st, x, K, signs, xq, sx);
 }
 
 }  // namespace tl

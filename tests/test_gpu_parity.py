@@ -181,6 +181,24 @@ def test_decode_prefill_agree(tl, M):
     _compare(L, acc_d, y_d, 4, frobenius=False)
 
 
+@pytest.mark.parametrize("K", [1024, 3072, 6144, 8192, 16384, 17408])
+def test_decode_m1_shapes(tl, K):
+    """M = 1 runs a kernel specialised on K / 1024 for the common depths, a generic one otherwise."""
+    L = synth.config_inputs("decode", M=1, N=384, K=K)
+    packed, qT, sw = pack_dev(tl, L)
+    acc, y = _run(tl, "decode", L, packed, qT, sw, 4)
+    _compare(L, acc, y, 4)
+
+
+@pytest.mark.parametrize("M,K", [(2, 17408), (7, 17408), (16, 17408), (32, 17408), (32, 1024)])
+def test_decode_slabs(tl, M, K):
+    """M * K beyond one shared-memory slab: K is processed in slabs with partial sums."""
+    L = synth.config_inputs("down_proj", M=M, N=256, K=K)
+    packed, qT, sw = pack_dev(tl, L)
+    acc, y = _run(tl, "decode", L, packed, qT, sw, 4)
+    _compare(L, acc, y, 4)
+
+
 @pytest.mark.parametrize("M,N,K", [(300, 384, 2048), (129, 256, 1024), (1, 128, 1024),
                                    (256, 640, 4096), (777, 128, 3072)])
 def test_prefill_ragged(tl, M, N, K):
