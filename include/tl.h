@@ -145,6 +145,37 @@ int tl_linear_decode(const uint8_t* packed, const int8_t* qT, const float* sw,
                      void* y, int y_dtype, int32_t* acc_dbg, void* stream);
 
 /*
+ * Bytes of the library-owned scratch array used by tl_linear_prefill_noalloc
+ * (8 MiB, held on every device that loads the library until the process exits).
+ */
+#define TL_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/*
+ * tl_linear_prefill without a caller workspace, for callers that cannot
+ * allocate device memory: a host program that has handed all device memory
+ * to its own pool (a serving engine that reserves the KV cache up front), or
+ * code that must not call cudaMalloc because it synchronises the device.
+ * (This entry point has no counterpart on the source pages; it only changes
+ * where the scratch lives.)
+ *
+ * Arguments, layout, result and errors are those of tl_linear_prefill. When
+ * the problem has few output tiles the K dimension is split and the partial
+ * int32 sums meet in a static device array of TL_NOALLOC_SCRATCH_BYTES owned
+ * by the library; the call clears the part it uses before the kernel. If that
+ * part would exceed the array (M * N * 4 bytes plus 4 bytes per output tile,
+ * see tl_prefill_workspace_size) the call returns TL_ENOSPACE and launches
+ * nothing. The call allocates nothing and calls no allocating routine.
+ *
+ * - Every call shares the one array per device: calls that can overlap on the
+ *   GPU (other streams, other host threads) race on it; serialise them.
+ * - The first call on a device looks up the array's device address; make that
+ *   first call before any stream capture.
+ */
+int tl_linear_prefill_noalloc(const uint8_t* packed, const int8_t* qT, const float* sw,
+                              const uint16_t* xq, const float* sx, int M, int N, int K,
+                              void* y, int y_dtype, int32_t* acc_dbg, void* stream);
+
+/*
  * Synchronises `stream`, then returns and clears the current device's status
  * word: TL_OK, TL_ETIMEOUT or TL_EDATA (first error recorded), or TL_ECUDA if
  * the synchronisation itself failed.

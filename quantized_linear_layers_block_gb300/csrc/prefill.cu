@@ -487,3 +487,29 @@ int launch_prefill(const PrefillArgs& a, int* status, cudaStream_t st, cudaError
 }
 
 }  // namespace tl
+
+// ------------------------------------------------------------------ library-owned scratch
+// Split-K scratch for tl_linear_prefill_noalloc: a fixed array that every
+// device loading this library holds until the process exits. Host code must
+// not pass the symbol itself to a kernel (on the host it is only a stand-in);
+// the device address is looked up once per device below.
+static __device__ __align__(256) unsigned char g_prefill_scratch[TL_NOALLOC_SCRATCH_BYTES];
+
+namespace tl {
+
+int prefill_noalloc_scratch(void** ptr) {
+  static void* cache[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TL_ECUDA;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_prefill_scratch) != cudaSuccess || p == nullptr) return TL_ECUDA;
+    cache[dev] = p;
+  }
+  *ptr = cache[dev];
+  return TL_OK;
+}
+
+}  // namespace tl

@@ -139,6 +139,24 @@ int tl_linear_prefill(const uint8_t* packed, const int8_t* qT, const float* sw,
   return tl::launch_prefill(a, status, as_stream(stream), &ce);
 }
 
+int tl_linear_prefill_noalloc(const uint8_t* packed, const int8_t* qT, const float* sw,
+                              const uint16_t* xq, const float* sx, int M, int N, int K, void* y,
+                              int y_dtype, int32_t* acc_dbg, void* stream) {
+  int r = check_linear(packed, qT, sw, xq, sx, M, N, K, y, y_dtype, acc_dbg);
+  if (r != TL_OK || M == 0 || N == 0) return r;
+  size_t need = 0;
+  if ((r = tl_prefill_workspace_size(M, N, K, &need)) != TL_OK) return r;
+  if (need > tl::kNoAllocScratchBytes) return TL_ENOSPACE;
+  int* status = nullptr;
+  if ((r = status_ptr(&status)) != TL_OK) return r;
+  void* scratch = nullptr;
+  if ((r = tl::prefill_noalloc_scratch(&scratch)) != TL_OK) return r;
+  tl::PrefillArgs a{packed, qT, sw, xq, sx, M, N, K, y, y_dtype, acc_dbg, scratch,
+                    tl::kNoAllocScratchBytes};
+  cudaError_t ce;
+  return tl::launch_prefill(a, status, as_stream(stream), &ce);
+}
+
 int tl_linear_decode(const uint8_t* packed, const int8_t* qT, const float* sw, const int8_t* xq,
                      const float* sx, int M, int N, int K, void* y, int y_dtype,
                      int32_t* acc_dbg, void* stream) {

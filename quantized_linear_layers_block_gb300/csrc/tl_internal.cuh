@@ -18,6 +18,7 @@ constexpr int kBlock = 1024;          // Hadamard block and integer-exact fp32 c
 constexpr int kGroup = 128;           // columns per fp16 weight scale
 constexpr int kMaxK = 32768;          // rotate_quant holds one warp per 1024-block
 constexpr int kMaxDecodeM = 32;
+constexpr size_t kNoAllocScratchBytes = TL_NOALLOC_SCRATCH_BYTES;
 
 // Bounded device waits give up after this many nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -58,6 +59,9 @@ cudaError_t launch_decode(const uint32_t* packed, const int8_t* qT, const float*
 size_t prefill_workspace_bytes(int M, int N, int K, int num_sms);
 // Returns TL_OK or a tl_status; *cerr receives the CUDA error when TL_ECUDA.
 int launch_prefill(const PrefillArgs& a, int* status, cudaStream_t st, cudaError_t* cerr);
+// Device address (this device) of the library-owned split-K scratch array of
+// kNoAllocScratchBytes; the first call on a device looks it up.
+int prefill_noalloc_scratch(void** ptr);
 
 // Launch with programmatic stream serialization (PDL) enabled and, when
 // cluster > 1, thread-block clusters of `cluster` CTAs along x.

@@ -35,6 +35,7 @@ SIGNATURES = {
     "tl_prefill_workspace_size": (_I, [_I, _I, _I, _PSZ]),
     "tl_linear_prefill": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P, _SZ, _P]),
     "tl_linear_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P]),
+    "tl_linear_prefill_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P]),
     "tl_get_status": (_I, [_P]),
 }
 
@@ -162,6 +163,24 @@ def tl_linear_prefill(packed, qT, sw, xq, sx, N: int, K: int, y_dtype: int = TL_
     _check(lib().tl_linear_prefill(_ptr(packed), _ptr(qT), _ptr(sw), _ptr(xq), _ptr(sx), M, N, K,
                                    _ptr(y), y_dtype, _ptr(acc_dbg), _ptr(workspace), ws_bytes,
                                    _stream(stream)), "tl_linear_prefill")
+    return y
+
+
+def tl_linear_prefill_noalloc(packed, qT, sw, xq, sx, N: int, K: int, y_dtype: int = TL_BF16,
+                              y: torch.Tensor | None = None, acc_dbg: torch.Tensor | None = None,
+                              stream=None) -> torch.Tensor:
+    """tl_linear_prefill with the library's own static split-K scratch (no workspace argument).
+
+    For callers that cannot allocate device memory; see include/tl.h. Calls
+    that may overlap on the GPU share the scratch and must be serialised.
+    """
+    _dev_tensor(xq, torch.float16, "xq")
+    M = xq.shape[0]
+    if y is None:
+        y = _linear_out(M, N, y_dtype, xq.device, y)
+    _check(lib().tl_linear_prefill_noalloc(_ptr(packed), _ptr(qT), _ptr(sw), _ptr(xq), _ptr(sx), M, N,
+                                           K, _ptr(y), y_dtype, _ptr(acc_dbg), _stream(stream)),
+           "tl_linear_prefill_noalloc")
     return y
 
 
