@@ -13,20 +13,30 @@
 // results are then converted to int32 and summed exactly. The int32 result
 // equals the int8 GEMM's bit for bit.
 //
-// Roles (one CTA per SM, persistent over output tiles of 128 weight rows x
-// 128 tokens; the MMA is D[n, m] = sum_k W[n, k] X[m, k], i.e. y transposed):
-//   warp 0      TMA producer: per 64-column stage, the fp16 activation tile
-//               (128-byte swizzle), the packed 2-bit codes of the 128 rows and
-//               their q bytes, into a 6-deep shared-memory ring.
-//   warp 1      allocates tensor memory; one thread issues the MMAs.
-//   warps 4-7   expansion: lane = weight row; decode 64 codes with q into 32
-//               fp16 pairs in registers and store them into tensor memory as
-//               the MMA's A operand (tcgen05.st), one 32-column slot per stage.
-//   warps 8-15  drain + epilogue: after each chunk read the fp32 accumulator
-//               (double buffered), add it to int32 totals in registers; at the
-//               end of a tile write y = (fl32(acc) sw[n]) sx[m].
-// Tensor memory (512 columns x 128 lanes): A slots at columns 32 s, the two
-// fp32 accumulators at columns 256 and 384.
+// Work: persistent CTAs (one per SM) over output tiles of 128 weight rows x
+// 128 tokens; the MMA computes D[n, m] = sum_k W[n, k] X[m, k] (y transposed,
+// weight rows on the tensor-memory lanes), 64 columns of K per stage.
+// Roles of the 20 warps:
+//   warp 0       weight producer: packed 2-bit codes of the 128 rows and their q
+//                bytes per stage into a 16-deep ring; it starts before the kernel
+//                waits for the preceding one (programmatic dependent launch).
+//   warp 2       activation producer: after that wait, the fp16 activation tile
+//                per stage (128-byte swizzle) into an 8-deep ring.
+//   warp 1       allocates tensor memory; one thread issues the MMAs.
+//   warps 4-11   expansion, two warps per 32-lane quarter of tensor memory taking
+//                alternate stages: lane = weight row; 64 codes and q become 32
+//                fp16 pairs in registers, stored into tensor memory as the MMA's A
+//                operand (tcgen05.st). A slot is refilled as soon as the MMA that
+//                read it completes (the MMA's commit releases it directly).
+//   warps 12-19  drain + epilogue, two per quarter (64 tokens each): after each
+//                chunk add the fp32 accumulator (double buffered) into int32
+//                totals in registers; at the end of a tile write
+//                y = (fl32(acc) sw[n]) sx[m].
+// Tensor memory (512 columns x 128 lanes): 8 A slots [0,256), fp32
+// accumulators [256,384) and [384,512).
+// The depth of each ring covers its recycling latency: an A slot goes round
+// MMA completion -> commit -> expansion -> MMA issue (two mbarrier hops plus
+// the expansion); a weight or activation slot adds the copy's latency.
 // When the problem has fewer tiles than SMs, K is split across CTAs; partial
 // int32 sums meet in a caller workspace and the last CTA of a tile finishes it.
 #include "tl_internal.cuh"
@@ -42,32 +52,39 @@ namespace {
 
 constexpr int BM = 128;             // weight rows per tile (MMA M, TMEM lanes)
 constexpr int BN = 128;             // tokens per tile (MMA N)
-constexpr int BK = 64;              // columns of K per pipeline stage
-constexpr int NST = 6;              // pipeline depth
+constexpr int BK = 128;             // columns of K per pipeline stage (= one q group)
+constexpr int HALF_K = 64;          // columns per 128-byte swizzled activation box
+constexpr int NW = 8;               // weight ring depth
+constexpr int NS = 4;               // stage ring depth (tensor-memory A slot + activation slot)
 constexpr int STAGES_PER_CHUNK = kBlock / BK;
 constexpr int UMMA_K = 16;
+constexpr int MMAS_PER_STAGE = BK / UMMA_K;
 
-constexpr int B_BYTES = BN * BK * 2;          // 16 KB fp16 activation tile
-constexpr int P_BYTES = BM * (BK / 4);        // 2 KB packed codes
+constexpr int B_BYTES = BN * BK * 2;          // 32 KB fp16 activation tile (two 16 KB boxes)
+constexpr int B_HALF = BN * HALF_K * 2;
+constexpr int P_BYTES = BM * (BK / 4);        // 4 KB packed codes
 constexpr int Q_BYTES = BM;                   // 128 q bytes
-constexpr uint32_t STAGE_TX = B_BYTES + P_BYTES + Q_BYTES;
+constexpr uint32_t W_TX = P_BYTES + Q_BYTES;
 
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t A_COL0 = 0;                // A slot s at columns 32 s
+constexpr uint32_t A_COLS = BK / 2;           // 64 columns of fp16 pairs per A slot
+constexpr uint32_t A_COL0 = 0;                // A slot s at columns 64 s
 constexpr uint32_t D_COL0 = 256;              // accumulators at 256 and 384
 
-constexpr int kThreads = 512;
-constexpr int WARP_TMA = 0, WARP_MMA = 1, WARP_EXP0 = 4, WARP_DRAIN0 = 8;
+constexpr int WARP_WLOAD = 0, WARP_MMA = 1, WARP_BLOAD = 2, WARP_EXP0 = 4, WARP_DRAIN0 = 12;
+constexpr int N_EXP_WARPS = 8, N_DRAIN_WARPS = 8;
+constexpr int kThreads = (WARP_DRAIN0 + N_DRAIN_WARPS) * 32;
 
 constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
 
 struct Smem {
   // byte offsets inside the 1024-aligned dynamic shared memory block
   static constexpr int b = 0;
-  static constexpr int p = b + NST * B_BYTES;
-  static constexpr int q = p + NST * P_BYTES;
-  static constexpr int bar = q + NST * Q_BYTES;     // 8-byte aligned
-  static constexpr int n_bars = 3 * NST + 2 + 2 + 3;
+  static constexpr int p = b + NS * B_BYTES;
+  static constexpr int q = p + NW * P_BYTES;
+  static constexpr int bar = q + NW * Q_BYTES;
+  // wfull[NW] wempty[NW] full[NS] empty[NS] dfull[2] dempty[2] fin rdv1 rdv2
+  static constexpr int n_bars = 2 * NW + 2 * NS + 2 + 2 + 3;
   static constexpr int misc = bar + n_bars * 8;
   static constexpr int total = misc + 16;
 };
@@ -116,6 +133,17 @@ __device__ __forceinline__ void expand_word(uint32_t w, __half2 q2, uint32_t* ou
   }
 }
 
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_p,
                const __grid_constant__ CUtensorMap map_q, const float* __restrict__ sw,
@@ -127,14 +155,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + Smem::bar;
-  auto full = [&](int s) { return bar0 + 8u * s; };
-  auto empty = [&](int s) { return bar0 + 8u * (NST + s); };
-  auto afull = [&](int s) { return bar0 + 8u * (2 * NST + s); };
-  auto dfull = [&](int b) { return bar0 + 8u * (3 * NST + b); };
-  auto dempty = [&](int b) { return bar0 + 8u * (3 * NST + 2 + b); };
-  const uint32_t fin = bar0 + 8u * (3 * NST + 4);
-  const uint32_t rdv1 = bar0 + 8u * (3 * NST + 5);
-  const uint32_t rdv2 = bar0 + 8u * (3 * NST + 6);
+  auto wfull = [&](int i) { return bar0 + 8u * i; };
+  auto wempty = [&](int i) { return bar0 + 8u * (NW + i); };
+  auto full = [&](int i) { return bar0 + 8u * (2 * NW + i); };
+  auto empty = [&](int i) { return bar0 + 8u * (2 * NW + NS + i); };
+  auto dfull = [&](int i) { return bar0 + 8u * (2 * NW + 2 * NS + i); };
+  auto dempty = [&](int i) { return bar0 + 8u * (2 * NW + 2 * NS + 2 + i); };
+  const uint32_t fin = bar0 + 8u * (2 * NW + 2 * NS + 4);
+  const uint32_t rdv1 = fin + 8u;
+  const uint32_t rdv2 = fin + 16u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Smem::misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem::misc + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + Smem::misc + 8);
@@ -143,17 +172,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(full(s), 1);
-      mbar_init(empty(s), 1);
-      mbar_init(afull(s), 4);
+    for (int i = 0; i < NW; ++i) {
+      mbar_init(wfull(i), 1);
+      mbar_init(wempty(i), 4);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(dfull(b), 1);
-      mbar_init(dempty(b), 8);
+    for (int i = 0; i < NS; ++i) {
+      // a stage is ready when its activation bytes have landed (producer's
+      // arrive + transaction count) and the 4 expansion warps have filled its
+      // tensor-memory A slot
+      mbar_init(full(i), 1 + 4);
+      mbar_init(empty(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(dfull(i), 1);
+      mbar_init(dempty(i), N_DRAIN_WARPS);
     }
     mbar_init(fin, 1);
-    mbar_init(rdv1, 8);
+    mbar_init(rdv1, N_DRAIN_WARPS);
     mbar_init(rdv2, 1);
     *abort_flag = 0;
     *last_flag = 0;
@@ -173,9 +208,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
     set_status(status, TL_ETIMEOUT);
   };
 
-  if (warp == WARP_TMA) {
+  if (warp == WARP_WLOAD) {
     if (lane == 0) {
-      tma_prefetch_desc(&map_x);
       tma_prefetch_desc(&map_p);
       tma_prefetch_desc(&map_q);
       uint32_t it = 0;
@@ -185,31 +219,66 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
         unit_coords(work, u, nt, mt, c0, c1);
         for (int c = c0; ok && c < c1; ++c) {
           for (int st = 0; st < STAGES_PER_CHUNK; ++st, ++it) {
-            const int s = it % NST;
-            const uint32_t ph = (it / NST) & 1u;
+            const int w = it % NW;
+            const uint32_t ph = (it / NW) & 1u;
+            if (!mbar_wait(wempty(w), ph ^ 1u, abort_flag)) {
+              fail();
+              ok = false;
+              break;
+            }
+            const int k0 = c * kBlock + st * BK;
+            mbar_arrive_expect_tx(wfull(w), W_TX);
+            tma_load_2d(sbase + Smem::p + w * P_BYTES, &map_p, k0 / 4, nt * BM, wfull(w));
+            tma_load_2d(sbase + Smem::q + w * Q_BYTES, &map_q, nt * BM, k0 / kGroup, wfull(w));
+          }
+        }
+      }
+      if (!ok) {
+        // let the copies already issued land before shared memory goes away
+        const uint32_t n = it < NW ? it : NW;
+        for (uint32_t i = it - n; i < it; ++i) mbar_wait(wfull(i % NW), (i / NW) & 1u, nullptr);
+      }
+    }
+  } else if (warp == WARP_BLOAD) {
+    if (lane == 0) {
+      tma_prefetch_desc(&map_x);
+      // the activations are written by the preceding kernel in the stream
+      pdl_wait_prior();
+      uint32_t it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < work.units; u += gridDim.x) {
+        int nt, mt, c0, c1;
+        unit_coords(work, u, nt, mt, c0, c1);
+        for (int c = c0; ok && c < c1; ++c) {
+          for (int st = 0; st < STAGES_PER_CHUNK; ++st, ++it) {
+            const int s = it % NS;
+            const uint32_t ph = (it / NS) & 1u;
             if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) {
               fail();
               ok = false;
               break;
             }
             const int k0 = c * kBlock + st * BK;
-            mbar_arrive_expect_tx(full(s), STAGE_TX);
+            mbar_arrive_expect_tx(full(s), B_BYTES);
             tma_load_2d(sbase + Smem::b + s * B_BYTES, &map_x, k0, mt * BN, full(s));
-            tma_load_2d(sbase + Smem::p + s * P_BYTES, &map_p, k0 / 4, nt * BM, full(s));
-            tma_load_2d(sbase + Smem::q + s * Q_BYTES, &map_q, nt * BM, k0 / kGroup, full(s));
+            tma_load_2d(sbase + Smem::b + s * B_BYTES + B_HALF, &map_x, k0 + HALF_K, mt * BN, full(s));
           }
         }
       }
+      pdl_launch_dependents();
       if (!ok) {
-        // let the copies already issued land before shared memory goes away
-        const uint32_t n = it < NST ? it : NST;
-        for (uint32_t i = it - n; i < it; ++i) mbar_wait(full(i % NST), (i / NST) & 1u, nullptr);
+        // bounded: the expansion arrivals of these stages may never come
+        const uint32_t n = it < NS ? it : NS;
+        for (uint32_t i = it - n; i < it; ++i) mbar_wait(full(i % NS), (i / NS) & 1u, nullptr);
       }
     }
   } else if (warp == WARP_MMA) {
     if (lane == 0) {
       uint32_t it = 0, cc = 0;
       bool ok = true;
+      // descriptor of activation slot 0, first 16 columns; slots are 32 KB apart,
+      // the second 64-column box 16 KB further, each 16-column step 32 bytes
+      const uint64_t desc0 = smem_desc_sw128(sbase + Smem::b);
       for (int u = blockIdx.x; ok && u < work.units; u += gridDim.x) {
         int nt, mt, c0, c1;
         unit_coords(work, u, nt, mt, c0, c1);
@@ -224,19 +293,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
           tc_fence_after();
           const uint32_t d_addr = tmem + D_COL0 + buf * BN;
           for (int st = 0; st < STAGES_PER_CHUNK; ++st, ++it) {
-            const int s = it % NST;
-            const uint32_t ph = (it / NST) & 1u;
-            if (!mbar_wait(full(s), ph, abort_flag) || !mbar_wait(afull(s), ph, abort_flag)) {
+            const int s = it % NS;
+            const uint32_t ph = (it / NS) & 1u;
+            if (!mbar_wait(full(s), ph, abort_flag)) {
               fail();
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t b_addr = sbase + Smem::b + s * B_BYTES;
+            const uint64_t dslot = desc0 + static_cast<uint64_t>((s * B_BYTES) >> 4);
+            const uint32_t aslot = tmem + A_COL0 + A_COLS * s;
 #pragma unroll
-            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-              mma_f16_ts(d_addr, tmem + A_COL0 + 32u * s + 8u * kk,
-                         smem_desc_sw128(b_addr + 32u * kk), IDESC, (st | kk) != 0);
+            for (int j = 0; j < MMAS_PER_STAGE; ++j) {
+              const uint32_t boff = (j >> 2) * (B_HALF >> 4) + (j & 3) * (32 >> 4);
+              mma_f16_ts(d_addr, aslot + 8u * j, dslot + boff, IDESC, (st | j) != 0);
             }
             tc_commit(empty(s));
           }
@@ -247,8 +317,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
       tc_commit(fin);
       mbar_wait(fin, 0, nullptr);
     }
-  } else if (warp >= WARP_EXP0 && warp < WARP_EXP0 + 4) {
+  } else if (warp >= WARP_EXP0 && warp < WARP_EXP0 + N_EXP_WARPS) {
     const int quarter = warp & 3;
+    const uint32_t mine = static_cast<uint32_t>((warp - WARP_EXP0) >> 2);   // stage parity
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     uint32_t it = 0;
@@ -258,29 +329,48 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
       unit_coords(work, u, nt, mt, c0, c1);
       for (int c = c0; ok && c < c1; ++c) {
         for (int st = 0; st < STAGES_PER_CHUNK; ++st, ++it) {
-          const int s = it % NST;
-          const uint32_t ph = (it / NST) & 1u;
-          const bool got = mbar_wait(full(s), ph, abort_flag) && mbar_wait(empty(s), ph ^ 1u, abort_flag);
+          if ((it & 1u) != mine) continue;
+          const int w = it % NW;
+          const uint32_t wph = (it / NW) & 1u;
+          const int s = it % NS;
+          const uint32_t ph = (it / NS) & 1u;
+          const bool got = mbar_wait(wfull(w), wph, abort_flag);
           if (!__all_sync(0xffffffffu, got)) {
             fail();
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint4 pk = *reinterpret_cast<const uint4*>(smem + Smem::p + s * P_BYTES + row * 16);
-          const int qv = static_cast<int8_t>(smem[Smem::q + s * Q_BYTES + row]);
+          const uint4* prow = reinterpret_cast<const uint4*>(smem + Smem::p + w * P_BYTES + row * 32);
+          const uint4 pk0 = prow[0], pk1 = prow[1];
+          const int qv = static_cast<int8_t>(smem[Smem::q + w * Q_BYTES + row]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(wempty(w));   // weight slot consumed
           const __half qh = __int2half_rn(qv);
           const __half2 q2 = __halves2half2(qh, qh);
           uint32_t out[32];
-          expand_word(pk.x, q2, out + 0);
-          expand_word(pk.y, q2, out + 8);
-          expand_word(pk.z, q2, out + 16);
-          expand_word(pk.w, q2, out + 24);
-          tmem_st_32x32b_x32(lane_base + A_COL0 + 32u * s, out);
+          expand_word(pk0.x, q2, out + 0);
+          expand_word(pk0.y, q2, out + 8);
+          expand_word(pk0.z, q2, out + 16);
+          expand_word(pk0.w, q2, out + 24);
+          // the A slot is free once the MMAs of the stage that used it last completed
+          const bool free_slot = mbar_wait(empty(s), ph ^ 1u, abort_flag);
+          if (!__all_sync(0xffffffffu, free_slot)) {
+            fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t aslot = lane_base + A_COL0 + A_COLS * s;
+          tmem_st_32x32b_x32(aslot, out);
+          expand_word(pk1.x, q2, out + 0);
+          expand_word(pk1.y, q2, out + 8);
+          expand_word(pk1.z, q2, out + 16);
+          expand_word(pk1.w, q2, out + 24);
+          tmem_st_32x32b_x32(aslot + 32, out);
           tmem_wait_st();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(afull(s));
+          if (lane == 0) mbar_arrive(full(s));
         }
       }
     }
@@ -308,12 +398,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
         }
         tc_fence_after();
 #pragma unroll
-        for (int p = 0; p < 2; ++p) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(lane_base + D_COL0 + buf * BN + half * 64 + p * 32, v);
+        for (int p = 0; p < 4; ++p) {
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(lane_base + D_COL0 + buf * BN + half * 64 + p * 16, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) tot[p * 32 + i] += __float2int_rn(__uint_as_float(v[i]));
+          for (int i = 0; i < 16; ++i) tot[p * 16 + i] += __float2int_rn(__uint_as_float(v[i]));
         }
         tc_fence_before();
         __syncwarp();
@@ -323,7 +413,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
       const int mbase = mt * BN + half * 64;
       bool finish = ok;
       if (work.split > 1) {
-        // Rendezvous of the 8 drain warps through two mbarriers (bounded waits):
+        // Rendezvous of the drain warps through two mbarriers (bounded waits):
         // every warp adds its partial sums, the leader counts the tile's
         // finished splits, and the CTA that completes the tile writes it.
         const uint32_t rp = ku & 1u;
@@ -448,7 +538,7 @@ int launch_prefill(const PrefillArgs& a, int* status, cudaStream_t st, cudaError
   const int G = a.K / kGroup;
   CUtensorMap mx, mp, mq;
   if (!make_map_2d(enc, &mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.xq, a.K, a.M,
-                   static_cast<uint64_t>(a.K) * 2, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                   static_cast<uint64_t>(a.K) * 2, HALF_K, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_2d(enc, &mp, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.packed, a.K / 4, a.N,
                    static_cast<uint64_t>(a.K) / 4, BK / 4, BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_map_2d(enc, &mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.qT, a.N, G, static_cast<uint64_t>(a.N),
@@ -480,9 +570,10 @@ int launch_prefill(const PrefillArgs& a, int* status, cudaStream_t st, cudaError
   if ((*cerr = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(smem))) != cudaSuccess)
     return TL_ECUDA;
-  prefill_kernel<<<grid, kThreads, smem, st>>>(mx, mp, mq, a.sw, a.sx, a.M, a.N, w, a.y,
-                                               a.y_dtype, a.acc_dbg, ws_acc, ws_cnt, status);
-  if ((*cerr = cudaGetLastError()) != cudaSuccess) return TL_ECUDA;
+  if ((*cerr = launch_pdl(prefill_kernel, dim3(grid), dim3(kThreads), smem, st, mx, mp, mq, a.sw,
+                          a.sx, a.M, a.N, w, a.y, a.y_dtype, a.acc_dbg, ws_acc, ws_cnt, status)) !=
+      cudaSuccess)
+    return TL_ECUDA;
   return TL_OK;
 }
 
