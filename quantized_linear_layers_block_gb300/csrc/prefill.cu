@@ -52,23 +52,24 @@ namespace {
 
 constexpr int BM = 128;             // weight rows per tile (MMA M, TMEM lanes)
 constexpr int BN = 128;             // tokens per tile (MMA N)
-constexpr int BK = 128;             // columns of K per pipeline stage (= one q group)
-constexpr int HALF_K = 64;          // columns per 128-byte swizzled activation box
-constexpr int NW = 8;               // weight ring depth
-constexpr int NS = 4;               // stage ring depth (tensor-memory A slot + activation slot)
+constexpr int BK = 256;             // columns of K per pipeline stage (two q groups)
+constexpr int BOX_K = 64;           // columns per 128-byte swizzled activation box
+constexpr int NW = 4;               // weight ring depth
+constexpr int NB = 3;               // activation ring depth
+constexpr int NA = 2;               // tensor-memory A slots
 constexpr int STAGES_PER_CHUNK = kBlock / BK;
 constexpr int UMMA_K = 16;
 constexpr int MMAS_PER_STAGE = BK / UMMA_K;
 
-constexpr int B_BYTES = BN * BK * 2;          // 32 KB fp16 activation tile (two 16 KB boxes)
-constexpr int B_HALF = BN * HALF_K * 2;
-constexpr int P_BYTES = BM * (BK / 4);        // 4 KB packed codes
-constexpr int Q_BYTES = BM;                   // 128 q bytes
+constexpr int BOX_BYTES = BN * BOX_K * 2;     // 16 KB
+constexpr int B_BYTES = BN * BK * 2;          // 64 KB fp16 activation tile (four boxes)
+constexpr int P_BYTES = BM * (BK / 4);        // 8 KB packed codes
+constexpr int Q_BYTES = BM * (BK / kGroup);   // 256 q bytes: [2 groups][128 rows]
 constexpr uint32_t W_TX = P_BYTES + Q_BYTES;
 
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t A_COLS = BK / 2;           // 64 columns of fp16 pairs per A slot
-constexpr uint32_t A_COL0 = 0;                // A slot s at columns 64 s
+constexpr uint32_t A_COLS = BK / 2;           // 128 columns of fp16 pairs per A slot
+constexpr uint32_t A_COL0 = 0;                // A slot a at columns 128 a
 constexpr uint32_t D_COL0 = 256;              // accumulators at 256 and 384
 
 constexpr int WARP_WLOAD = 0, WARP_MMA = 1, WARP_BLOAD = 2, WARP_EXP0 = 4, WARP_DRAIN0 = 12;
@@ -80,14 +81,15 @@ constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
 struct Smem {
   // byte offsets inside the 1024-aligned dynamic shared memory block
   static constexpr int b = 0;
-  static constexpr int p = b + NS * B_BYTES;
+  static constexpr int p = b + NB * B_BYTES;
   static constexpr int q = p + NW * P_BYTES;
   static constexpr int bar = q + NW * Q_BYTES;
-  // wfull[NW] wempty[NW] full[NS] empty[NS] dfull[2] dempty[2] fin rdv1 rdv2
-  static constexpr int n_bars = 2 * NW + 2 * NS + 2 + 2 + 3;
+  // wfull[NW] wempty[NW] bfull[NB] bempty[NB] afull[NA] aempty[NA] dfull[2] dempty[2] fin rdv1 rdv2
+  static constexpr int n_bars = 2 * NW + 2 * NB + 2 * NA + 2 + 2 + 3;
   static constexpr int misc = bar + n_bars * 8;
   static constexpr int total = misc + 16;
 };
+static_assert(Smem::total + 1024 <= 232448, "shared memory budget");
 
 struct Work {
   int units, split, mtiles, chunks;
@@ -157,11 +159,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
   const uint32_t bar0 = sbase + Smem::bar;
   auto wfull = [&](int i) { return bar0 + 8u * i; };
   auto wempty = [&](int i) { return bar0 + 8u * (NW + i); };
-  auto full = [&](int i) { return bar0 + 8u * (2 * NW + i); };
-  auto empty = [&](int i) { return bar0 + 8u * (2 * NW + NS + i); };
-  auto dfull = [&](int i) { return bar0 + 8u * (2 * NW + 2 * NS + i); };
-  auto dempty = [&](int i) { return bar0 + 8u * (2 * NW + 2 * NS + 2 + i); };
-  const uint32_t fin = bar0 + 8u * (2 * NW + 2 * NS + 4);
+  auto bfull = [&](int i) { return bar0 + 8u * (2 * NW + i); };
+  auto bempty = [&](int i) { return bar0 + 8u * (2 * NW + NB + i); };
+  auto afull = [&](int i) { return bar0 + 8u * (2 * NW + 2 * NB + i); };
+  auto aempty = [&](int i) { return bar0 + 8u * (2 * NW + 2 * NB + NA + i); };
+  auto dfull = [&](int i) { return bar0 + 8u * (2 * NW + 2 * NB + 2 * NA + i); };
+  auto dempty = [&](int i) { return bar0 + 8u * (2 * NW + 2 * NB + 2 * NA + 2 + i); };
+  const uint32_t fin = bar0 + 8u * (2 * NW + 2 * NB + 2 * NA + 4);
   const uint32_t rdv1 = fin + 8u;
   const uint32_t rdv2 = fin + 16u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Smem::misc);
@@ -174,14 +178,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
   if (threadIdx.x == 0) {
     for (int i = 0; i < NW; ++i) {
       mbar_init(wfull(i), 1);
-      mbar_init(wempty(i), 4);
+      mbar_init(wempty(i), N_EXP_WARPS);
     }
-    for (int i = 0; i < NS; ++i) {
-      // a stage is ready when its activation bytes have landed (producer's
-      // arrive + transaction count) and the 4 expansion warps have filled its
-      // tensor-memory A slot
-      mbar_init(full(i), 1 + 4);
-      mbar_init(empty(i), 1);
+    for (int i = 0; i < NB; ++i) {
+      mbar_init(bfull(i), 1);
+      mbar_init(bempty(i), 1);
+    }
+    for (int i = 0; i < NA; ++i) {
+      // a stage is ready for the MMAs when all 8 expansion warps have written
+      // their half of its A slot and have seen its activation tile land
+      mbar_init(afull(i), N_EXP_WARPS);
+      mbar_init(aempty(i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(dfull(i), 1);
@@ -251,33 +258,34 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
         unit_coords(work, u, nt, mt, c0, c1);
         for (int c = c0; ok && c < c1; ++c) {
           for (int st = 0; st < STAGES_PER_CHUNK; ++st, ++it) {
-            const int s = it % NS;
-            const uint32_t ph = (it / NS) & 1u;
-            if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) {
+            const int b = it % NB;
+            const uint32_t ph = (it / NB) & 1u;
+            if (!mbar_wait(bempty(b), ph ^ 1u, abort_flag)) {
               fail();
               ok = false;
               break;
             }
             const int k0 = c * kBlock + st * BK;
-            mbar_arrive_expect_tx(full(s), B_BYTES);
-            tma_load_2d(sbase + Smem::b + s * B_BYTES, &map_x, k0, mt * BN, full(s));
-            tma_load_2d(sbase + Smem::b + s * B_BYTES + B_HALF, &map_x, k0 + HALF_K, mt * BN, full(s));
+            mbar_arrive_expect_tx(bfull(b), B_BYTES);
+#pragma unroll
+            for (int bx = 0; bx < BK / BOX_K; ++bx)
+              tma_load_2d(sbase + Smem::b + b * B_BYTES + bx * BOX_BYTES, &map_x, k0 + bx * BOX_K,
+                          mt * BN, bfull(b));
           }
         }
       }
       pdl_launch_dependents();
       if (!ok) {
-        // bounded: the expansion arrivals of these stages may never come
-        const uint32_t n = it < NS ? it : NS;
-        for (uint32_t i = it - n; i < it; ++i) mbar_wait(full(i % NS), (i / NS) & 1u, nullptr);
+        const uint32_t n = it < NB ? it : NB;
+        for (uint32_t i = it - n; i < it; ++i) mbar_wait(bfull(i % NB), (i / NB) & 1u, nullptr);
       }
     }
   } else if (warp == WARP_MMA) {
     if (lane == 0) {
       uint32_t it = 0, cc = 0;
       bool ok = true;
-      // descriptor of activation slot 0, first 16 columns; slots are 32 KB apart,
-      // the second 64-column box 16 KB further, each 16-column step 32 bytes
+      // descriptor of activation slot 0, first box, first 16 columns: boxes are
+      // 16 KB apart, slots 64 KB apart, and each 16-column step is 32 bytes
       const uint64_t desc0 = smem_desc_sw128(sbase + Smem::b);
       for (int u = blockIdx.x; ok && u < work.units; u += gridDim.x) {
         int nt, mt, c0, c1;
@@ -293,22 +301,26 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
           tc_fence_after();
           const uint32_t d_addr = tmem + D_COL0 + buf * BN;
           for (int st = 0; st < STAGES_PER_CHUNK; ++st, ++it) {
-            const int s = it % NS;
-            const uint32_t ph = (it / NS) & 1u;
-            if (!mbar_wait(full(s), ph, abort_flag)) {
+            const int b = it % NB;
+            const int a = it % NA;
+            const uint32_t aph = (it / NA) & 1u;
+            // one wait per 16 MMAs: the expansion warps arrive only after the
+            // stage's activation tile has landed as well
+            if (!mbar_wait(afull(a), aph, abort_flag)) {
               fail();
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint64_t dslot = desc0 + static_cast<uint64_t>((s * B_BYTES) >> 4);
-            const uint32_t aslot = tmem + A_COL0 + A_COLS * s;
+            const uint64_t dslot = desc0 + static_cast<uint64_t>((b * B_BYTES) >> 4);
+            const uint32_t aslot = tmem + A_COL0 + A_COLS * a;
 #pragma unroll
             for (int j = 0; j < MMAS_PER_STAGE; ++j) {
-              const uint32_t boff = (j >> 2) * (B_HALF >> 4) + (j & 3) * (32 >> 4);
+              const uint32_t boff = (j >> 2) * (BOX_BYTES >> 4) + (j & 3) * (32 >> 4);
               mma_f16_ts(d_addr, aslot + 8u * j, dslot + boff, IDESC, (st | j) != 0);
             }
-            tc_commit(empty(s));
+            tc_commit(aempty(a));
+            tc_commit(bempty(b));
           }
           if (ok) tc_commit(dfull(buf));
         }
@@ -318,8 +330,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
       mbar_wait(fin, 0, nullptr);
     }
   } else if (warp >= WARP_EXP0 && warp < WARP_EXP0 + N_EXP_WARPS) {
+    // two warps per lane quarter; warp `part` expands columns [128 part, 128 part + 128)
+    // of every stage, i.e. q group `part` of the stage
     const int quarter = warp & 3;
-    const uint32_t mine = static_cast<uint32_t>((warp - WARP_EXP0) >> 2);   // stage parity
+    const int part = (warp - WARP_EXP0) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     uint32_t it = 0;
@@ -329,20 +343,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
       unit_coords(work, u, nt, mt, c0, c1);
       for (int c = c0; ok && c < c1; ++c) {
         for (int st = 0; st < STAGES_PER_CHUNK; ++st, ++it) {
-          if ((it & 1u) != mine) continue;
           const int w = it % NW;
           const uint32_t wph = (it / NW) & 1u;
-          const int s = it % NS;
-          const uint32_t ph = (it / NS) & 1u;
+          const int a = it % NA;
+          const uint32_t aph = (it / NA) & 1u;
+          const int b = it % NB;
+          const uint32_t bph = (it / NB) & 1u;
           const bool got = mbar_wait(wfull(w), wph, abort_flag);
           if (!__all_sync(0xffffffffu, got)) {
             fail();
             ok = false;
             break;
           }
-          const uint4* prow = reinterpret_cast<const uint4*>(smem + Smem::p + w * P_BYTES + row * 32);
+          const uint4* prow =
+              reinterpret_cast<const uint4*>(smem + Smem::p + w * P_BYTES + row * (BK / 4) + part * 32);
           const uint4 pk0 = prow[0], pk1 = prow[1];
-          const int qv = static_cast<int8_t>(smem[Smem::q + w * Q_BYTES + row]);
+          const int qv = static_cast<int8_t>(smem[Smem::q + w * Q_BYTES + part * BM + row]);
           __syncwarp();
           if (lane == 0) mbar_arrive(wempty(w));   // weight slot consumed
           const __half qh = __int2half_rn(qv);
@@ -353,14 +369,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
           expand_word(pk0.z, q2, out + 16);
           expand_word(pk0.w, q2, out + 24);
           // the A slot is free once the MMAs of the stage that used it last completed
-          const bool free_slot = mbar_wait(empty(s), ph ^ 1u, abort_flag);
+          const bool free_slot = mbar_wait(aempty(a), aph ^ 1u, abort_flag);
           if (!__all_sync(0xffffffffu, free_slot)) {
             fail();
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t aslot = lane_base + A_COL0 + A_COLS * s;
+          const uint32_t aslot = lane_base + A_COL0 + A_COLS * a + 64u * part;
           tmem_st_32x32b_x32(aslot, out);
           expand_word(pk1.x, q2, out + 0);
           expand_word(pk1.y, q2, out + 8);
@@ -369,8 +385,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
           tmem_st_32x32b_x32(aslot + 32, out);
           tmem_wait_st();
           tc_fence_before();
+          const bool landed = mbar_wait(bfull(b), bph, abort_flag);
+          if (!__all_sync(0xffffffffu, landed)) {
+            fail();
+            ok = false;
+            break;
+          }
           __syncwarp();
-          if (lane == 0) mbar_arrive(full(s));
+          if (lane == 0) mbar_arrive(afull(a));
         }
       }
     }
@@ -538,11 +560,11 @@ int launch_prefill(const PrefillArgs& a, int* status, cudaStream_t st, cudaError
   const int G = a.K / kGroup;
   CUtensorMap mx, mp, mq;
   if (!make_map_2d(enc, &mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.xq, a.K, a.M,
-                   static_cast<uint64_t>(a.K) * 2, HALF_K, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                   static_cast<uint64_t>(a.K) * 2, BOX_K, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_2d(enc, &mp, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.packed, a.K / 4, a.N,
                    static_cast<uint64_t>(a.K) / 4, BK / 4, BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_map_2d(enc, &mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.qT, a.N, G, static_cast<uint64_t>(a.N),
-                   BM, 1, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+                   BM, BK / kGroup, CU_TENSOR_MAP_SWIZZLE_NONE)) {
     return TL_EINVAL;
   }
 
