@@ -9,8 +9,10 @@ Metric: "ternary linear int8 TOPS @M=512; decode GEMV weight-stream GB/s @M=1".
            its weights in the 129 MB L2): per layer rotate+quantise (K1) then the
            tensor-core GEMM with fused rescale (K3). TOPS = 64 * 2 M N K / step.
   decode   (`decode` object): M=1, K=5120, N=17408 over 64 layer buffers (1.47 GB);
-           per layer K1 then the CUDA-core GEMV (K2), captured in one CUDA graph
-           per step. GB/s = 64 * (packed + qT + sw bytes) / step.
+           per layer rotate+quantise (K1) then the dp4a GEMV (K2), captured in one
+           CUDA graph per step. GB/s = 64 * (packed + qT + sw bytes) / step. The
+           GEMV kernel alone (64 back-to-back launches) gives the roofline figure;
+           the single-launch fused variant (tl_linear_decode_fused) is timed beside it.
 
 Inputs are seeded synthetic draws with the workloads' shapes and distributions,
 generated on the device; they are resident in HBM before timing starts.
@@ -281,6 +283,7 @@ def main(argv=None):
             ev[1].record(stream)
 
     def decode_layer(li):
+        # the decode step: rotate+quantise (K1), then the GEMV (K2)
         lay, x, y = dec_layers[li]
         tl.tl_rotate_quant_act(x, xq_dtype=tl.TL_I8, xq=xq_d, sx=sx_d)
         tl.tl_linear_decode(lay.packed, lay.qT, lay.sw, xq_d, sx_d, D["N"], D["K"], tl.TL_BF16, y=y)
@@ -288,6 +291,10 @@ def main(argv=None):
     def decode_kernel_only(li):
         lay, _, y = dec_layers[li]
         tl.tl_linear_decode(lay.packed, lay.qT, lay.sw, xq_d, sx_d, D["N"], D["K"], tl.TL_BF16, y=y)
+
+    def decode_fused(li):
+        lay, x, y = dec_layers[li]
+        tl.tl_linear_decode_fused(lay.packed, lay.qT, lay.sw, x, D["N"], D["K"], tl.TL_BF16, y=y)
 
     # warm-up (also resolves driver entry points and kernel attributes before capture)
     for _ in range(args.warmup):
@@ -298,15 +305,20 @@ def main(argv=None):
 
     g_dec = torch.cuda.CUDAGraph()
     g_dk = torch.cuda.CUDAGraph()
+    g_df = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_dec, capture_error_mode="relaxed"):
         for li in range(LAYERS):
             decode_layer(li)
     with torch.cuda.graph(g_dk, capture_error_mode="relaxed"):
         for li in range(LAYERS):
             decode_kernel_only(li)
+    with torch.cuda.graph(g_df, capture_error_mode="relaxed"):
+        for li in range(LAYERS):
+            decode_fused(li)
     for _ in range(args.warmup):
         g_dec.replay()
         g_dk.replay()
+        g_df.replay()
     torch.cuda.synchronize()
     if tl.tl_get_status() != tl.TL_OK:
         raise RuntimeError("device status after warm-up")
@@ -347,14 +359,19 @@ def main(argv=None):
     dec_ms = max_over_ranks(t_start.elapsed_time(t_end))
     clk = clocks.stop()
 
-    # kernel-only decode time (graph of back-to-back K2 launches)
+    # the GEMV kernel alone, 64 back-to-back launches on the layer buffers: its
+    # average duration is the roofline figure; then the fused single-launch layer
+    def graph_us(g, reps):
+        t_start.record(stream)
+        for _ in range(reps):
+            g.replay()
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        return 1e3 * t_start.elapsed_time(t_end) / (reps * LAYERS)
+
     reps = max(8, Kd // 4)
-    t_start.record(stream)
-    for _ in range(reps):
-        g_dk.replay()
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    k2_ms = t_start.elapsed_time(t_end) / (reps * LAYERS)
+    k2_ms = graph_us(g_dk, reps) * 1e-3
+    fused_us = graph_us(g_df, reps)
     status = tl.tl_get_status()
     if status != tl.TL_OK:
         raise RuntimeError(f"device status after timing: {tl.tl_strerror(status)}")
@@ -402,10 +419,11 @@ def main(argv=None):
                                     "kind::f16 tensor cores; fp16 and bf16 share the rate)"},
         "decode": {
             "metric": "decode GEMV weight-stream GB/s @M=1", "value": gbs, "unit": "GB/s",
-            "steps": Kd, "ms_per_step": dec_ms / Kd, "kernel_us": k2_ms * 1e3,
+            "steps": Kd, "ms_per_step": dec_ms / Kd, "layer_us": dec_ms * 1e3 / (Kd * LAYERS),
+            "kernel_us": k2_ms * 1e3, "fused_layer_us": fused_us,
             "roofline": {"bound": "hbm", "achieved": k2_gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": k2_gbs / hbm_peak, "traffic": traffic.get("decode_kernel"),
-                         "kernel": "decode kernel M=1 (K2), graph of back-to-back launches",
+                         "kernel": "decode1_kernel (K2) M=1, graph of 64 back-to-back launches",
                          "peak_source": f"{peak_src} hbm_gbs"},
             "e2e": {"value": ws * e2e_dsteps * LAYERS * wb / e2e_dec_s / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": LAYERS * D["M"] * D["K"] * 2,

@@ -145,6 +145,26 @@ int tl_linear_decode(const uint8_t* packed, const int8_t* qT, const float* sw,
                      void* y, int y_dtype, int32_t* acc_dbg, void* stream);
 
 /*
+ * Decode of one token (M = 1) with the input-side rotation and per-token
+ * quantisation done inside the GEMV kernel: equivalent, bit for bit, to
+ * tl_rotate_quant_act(x, TL_I8) followed by tl_linear_decode, in one launch
+ * (Qiita item ecc183fae033565af7cb: 前提 for the rotation, §4 for the per-token
+ * int8 and the row/token rescale, §5 for the dp4a decode GEMV).
+ *
+ *   x        bf16 bit patterns [1, K], K <= 8192; signs optional int8 [K] (+1/-1)
+ *   xq_out   optional int8 [K] receiving the quantised token (NULL: not written)
+ *   sx_out   optional fp32 [1] receiving the token scale (NULL: not written)
+ *   other arguments as for tl_linear_decode. M = 0 is a no-op; M > 1 or
+ *   K > 8192 returns TL_EUNSUPPORTED.
+ * Every CTA rotates the token itself, so x must be complete when the kernel
+ * starts reading it (it waits for the preceding kernel in the stream first).
+ */
+int tl_linear_decode_fused(const uint8_t* packed, const int8_t* qT, const float* sw,
+                           const uint16_t* x, const int8_t* signs, int M, int N, int K, void* y,
+                           int y_dtype, int32_t* acc_dbg, int8_t* xq_out, float* sx_out,
+                           void* stream);
+
+/*
  * Bytes of the library-owned scratch array used by tl_linear_prefill_noalloc
  * (8 MiB, held on every device that loads the library until the process exits).
  */

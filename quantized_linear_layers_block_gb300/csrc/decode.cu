@@ -160,6 +160,151 @@ decode1_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ q
   }
 }
 
+// ---------------------------------------------------------------- M = 1, fused
+// One launch for the whole layer at M = 1: the kernel takes the bf16 token,
+// and every CTA performs the input-side rotation and the per-token
+// quantisation itself (one warp per 1024-block, the same arithmetic as
+// tl_rotate_quant_act) before the GEMV. To keep that redundant rotation rare
+// the grid is one 1024-thread CTA per SM: CTA c owns a balanced, contiguous
+// range of 4-row quads (at most 32, one per warp), so each SM rotates the token
+// once. The dot product takes two masks per packed word instead of four
+// shift-and-mask pairs (fields 0 and 2 at scale 1, fields 1 and 3 at scale 4:
+// sum = P + Q/4, exact since Q is a multiple of 4), and a warp reduces its four
+// row sums together (two exchange steps that halve the rows, then three
+// butterfly steps).
+__device__ __forceinline__ int dot_chunk2(uint32_t wa, uint32_t wb, uint4 xa, uint4 xb, int t) {
+  const uint32_t wa4 = wa >> 4, wb4 = wb >> 4;
+  int p = t, q = 0;
+  p = __dp4a(static_cast<int>(wa & 0x03030303u), static_cast<int>(xa.x), p);
+  q = __dp4a(static_cast<int>(wa & 0x0C0C0C0Cu), static_cast<int>(xa.y), q);
+  p = __dp4a(static_cast<int>(wa4 & 0x03030303u), static_cast<int>(xa.z), p);
+  q = __dp4a(static_cast<int>(wa4 & 0x0C0C0C0Cu), static_cast<int>(xa.w), q);
+  p = __dp4a(static_cast<int>(wb & 0x03030303u), static_cast<int>(xb.x), p);
+  q = __dp4a(static_cast<int>(wb & 0x0C0C0C0Cu), static_cast<int>(xb.y), q);
+  p = __dp4a(static_cast<int>(wb4 & 0x03030303u), static_cast<int>(xb.z), p);
+  q = __dp4a(static_cast<int>(wb4 & 0x0C0C0C0Cu), static_cast<int>(xb.w), q);
+  return p + (q >> 2);
+}
+
+constexpr int kFusedWarps = 32;
+constexpr int kFusedMaxQuads = kFusedWarps;
+constexpr int kFusedQStride = 4 * (kFusedMaxQuads + 1);   // odd word count: conflict-free q reads
+
+template <int PL>
+__global__ void __launch_bounds__(kFusedWarps * 32, 1)
+decode1f_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ qT,
+                const float* __restrict__ sw, const uint16_t* __restrict__ x,
+                const int8_t* __restrict__ signs, int N, void* __restrict__ y, int y_dtype,
+                int32_t* __restrict__ acc_dbg, int8_t* __restrict__ xq_out,
+                float* __restrict__ sx_out) {
+  constexpr int K = PL * kBlock;
+  constexpr int G = K / kGroup;
+  constexpr int NC = K / 32;
+  // rows of weights in flight per warp; the rotation's 32 values per lane share the registers
+  constexpr int RR = PL <= 2 ? 4 : (PL <= 5 ? 2 : 1);
+  __shared__ __align__(16) uint4 xw0[NC];
+  __shared__ __align__(16) uint4 xw1[NC];
+  __shared__ int csum[NC];
+  __shared__ __align__(16) int8_t xnat[K];              // quantised token, natural order
+  __shared__ float bmax[PL];
+  __shared__ __align__(16) int8_t qs[G * kFusedQStride];  // q of the CTA's rows, [group][row]
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int Q = N >> 2;
+  const int q0 = static_cast<int>(static_cast<long long>(blockIdx.x) * Q / gridDim.x);
+  const int nq = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * Q / gridDim.x) - q0;
+  const int nb = 4 * q0;                                 // first row of the CTA
+  const int j = warp;                                    // this warp's quad
+  const uint2* pq = reinterpret_cast<const uint2*>(packed) + static_cast<size_t>(nb + 4 * j) * NC + lane;
+
+  uint2 ring[RR][PL];
+  if (j < nq) {
+#pragma unroll
+    for (int r = 0; r < RR; ++r) {
+#pragma unroll
+      for (int i = 0; i < PL; ++i) ring[r][i] = __ldg(pq + r * NC + i * 32);
+    }
+  }
+  pdl_launch_dependents();
+  for (int i = tid; i < G * nq; i += blockDim.x) {
+    const int g = i / nq, jq = i - g * nq;
+    *reinterpret_cast<uint32_t*>(qs + g * kFusedQStride + 4 * jq) =
+        __ldg(reinterpret_cast<const uint32_t*>(qT + static_cast<size_t>(g) * N + nb + 4 * jq));
+  }
+  pdl_wait_prior();
+
+  float v[4][8];
+  if (warp < PL) {
+    float am = rotate_block_warp(x + warp * kBlock, signs == nullptr ? nullptr : signs + warp * kBlock,
+                                 lane, v);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    if (lane == 0) bmax[warp] = am;
+  }
+  __syncthreads();
+  float a = 0.f;
+#pragma unroll
+  for (int b = 0; b < PL; ++b) a = fmaxf(a, bmax[b]);
+  const float inv = a > 0.f ? __fdiv_rn(127.f, a) : 0.f;
+  const float sx0 = a > 0.f ? __fdiv_rn(a, 127.f) : 0.f;
+  if (warp < PL) {
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      int q8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) q8[e] = quant_i8(v[jj][e], inv);
+      uint2 o;
+      o.x = (q8[0] & 0xFF) | ((q8[1] & 0xFF) << 8) | ((q8[2] & 0xFF) << 16) | ((q8[3] & 0xFF) << 24);
+      o.y = (q8[4] & 0xFF) | ((q8[5] & 0xFF) << 8) | ((q8[6] & 0xFF) << 16) | ((q8[7] & 0xFF) << 24);
+      const int off = warp * kBlock + 256 * jj + 8 * lane;
+      *reinterpret_cast<uint2*>(xnat + off) = o;
+      if (xq_out != nullptr && blockIdx.x == 0) *reinterpret_cast<uint2*>(xq_out + off) = o;
+    }
+  }
+  if (sx_out != nullptr && blockIdx.x == 0 && tid == 0) sx_out[0] = sx0;
+  __syncthreads();
+  for (int c = tid; c < NC; c += blockDim.x) {
+    const uint4* src = reinterpret_cast<const uint4*>(xnat + 32 * c);
+    uint4 p0, p1;
+    csum[c] = permute_chunk(src[0], src[1], p0, p1);
+    xw0[c] = p0;
+    xw1[c] = p1;
+  }
+  __syncthreads();
+  if (j >= nq) return;
+
+  int acc[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    int t_acc = 0;
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+      const int c = i * 32 + lane;
+      const uint2 wv = ring[r % RR][i];
+      if (r + RR < 4) ring[r % RR][i] = __ldg(pq + (r + RR) * NC + i * 32);
+      const int t = dot_chunk2(wv.x, wv.y, xw0[c], xw1[c], -csum[c]);
+      t_acc += static_cast<int>(qs[(8 * i + (lane >> 2)) * kFusedQStride + 4 * j + r]) * t;
+    }
+    acc[r] = t_acc;
+  }
+  // lanes with bit 4 clear keep rows 0, 1 and those with it set rows 2, 3; then
+  // bit 3 picks one of the two; lanes 0, 8, 16, 24 end with rows 0, 1, 2, 3.
+  const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0;
+  const int s0 = (b4 ? acc[2] : acc[0]) + __shfl_xor_sync(0xffffffffu, b4 ? acc[0] : acc[2], 16);
+  const int s1 = (b4 ? acc[3] : acc[1]) + __shfl_xor_sync(0xffffffffu, b4 ? acc[1] : acc[3], 16);
+  int s = (b3 ? s1 : s0) + __shfl_xor_sync(0xffffffffu, b3 ? s0 : s1, 8);
+  s += __shfl_xor_sync(0xffffffffu, s, 4);
+  s += __shfl_xor_sync(0xffffffffu, s, 2);
+  s += __shfl_xor_sync(0xffffffffu, s, 1);
+  if ((lane & 7) == 0) {
+    const int n = nb + 4 * j + 2 * (lane >> 4) + ((lane >> 3) & 1);
+    if (acc_dbg != nullptr) acc_dbg[n] = s;
+    store_y(y, y_dtype, n, __fmul_rn(__fmul_rn(__int2float_rn(s), sw[n]), sx0));
+  }
+}
+
 // ---------------------------------------------------------------- 1 <= M <= 32
 // MT tokens per pass (M rounded up to a power of two). A warp walks its
 // (row, chunk) items in order and keeps PF weight loads in flight; the first
@@ -332,6 +477,21 @@ cudaError_t launch_m1(const uint32_t* packed, const int8_t* qT, const float* sw,
                     packed, qT, sw, xq, sx, N, y, y_dtype, acc_dbg);
 }
 
+template <int PL>
+cudaError_t launch_m1f(const uint32_t* packed, const int8_t* qT, const float* sw, const uint16_t* x,
+                       const int8_t* signs, int N, void* y, int y_dtype, int32_t* acc_dbg,
+                       int8_t* xq_out, float* sx_out, cudaStream_t st) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int quads = N / 4;
+  int grid = (quads + kFusedMaxQuads - 1) / kFusedMaxQuads;   // at most 32 quads per CTA
+  if (grid < sms) grid = sms < quads ? sms : quads;
+  return launch_pdl(decode1f_kernel<PL>, dim3(grid), dim3(kFusedWarps * 32), 0, st, packed, qT, sw,
+                    x, signs, N, y, y_dtype, acc_dbg, xq_out, sx_out);
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const uint32_t* packed, const int8_t* qT, const float* sw,
@@ -356,6 +516,23 @@ cudaError_t launch_decode(const uint32_t* packed, const int8_t* qT, const float*
   if (M <= 8) return launch_mt<8>(packed, qT, sw, xq, sx, M, N, K, y, y_dtype, acc_dbg, st);
   if (M <= 16) return launch_mt<16>(packed, qT, sw, xq, sx, M, N, K, y, y_dtype, acc_dbg, st);
   return launch_mt<32>(packed, qT, sw, xq, sx, M, N, K, y, y_dtype, acc_dbg, st);
+}
+
+cudaError_t launch_decode_fused(const uint32_t* packed, const int8_t* qT, const float* sw,
+                                const uint16_t* x, const int8_t* signs, int N, int K, void* y,
+                                int y_dtype, int32_t* acc_dbg, int8_t* xq_out, float* sx_out,
+                                cudaStream_t st) {
+  switch (K / kBlock) {
+    case 1: return launch_m1f<1>(packed, qT, sw, x, signs, N, y, y_dtype, acc_dbg, xq_out, sx_out, st);
+    case 2: return launch_m1f<2>(packed, qT, sw, x, signs, N, y, y_dtype, acc_dbg, xq_out, sx_out, st);
+    case 3: return launch_m1f<3>(packed, qT, sw, x, signs, N, y, y_dtype, acc_dbg, xq_out, sx_out, st);
+    case 4: return launch_m1f<4>(packed, qT, sw, x, signs, N, y, y_dtype, acc_dbg, xq_out, sx_out, st);
+    case 5: return launch_m1f<5>(packed, qT, sw, x, signs, N, y, y_dtype, acc_dbg, xq_out, sx_out, st);
+    case 6: return launch_m1f<6>(packed, qT, sw, x, signs, N, y, y_dtype, acc_dbg, xq_out, sx_out, st);
+    case 7: return launch_m1f<7>(packed, qT, sw, x, signs, N, y, y_dtype, acc_dbg, xq_out, sx_out, st);
+    case 8: return launch_m1f<8>(packed, qT, sw, x, signs, N, y, y_dtype, acc_dbg, xq_out, sx_out, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace tl

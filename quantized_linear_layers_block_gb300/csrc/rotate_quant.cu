@@ -5,25 +5,15 @@
 // butterfly stage combines the two 512-halves) and §4 "効いた高速化"
 // (activations quantised to int8 per token after the rotation).
 //
-// One CTA per token, one warp per 1024-column block. Lane l holds the 32
-// elements i = 256 j + 8 l + e (j = 0..3, e = 0..7), loaded as four
-// coalesced 16-byte vectors. Butterfly strides 1, 2, 4 act on e (registers),
-// 8..128 on the lane index (warp shuffles), 256 and 512 on j (registers), so
-// the stages run in the order 1, 2, 4, ..., 512 and every element sees the
-// same fp32 additions as a plain sequential FWHT.
+// One CTA per token, one warp per 1024-column block (rotate_block_warp in
+// tl_internal.cuh: the butterfly stages run in the order 1, 2, 4, ..., 512, so
+// every element sees the same fp32 additions as a plain sequential FWHT).
 #include "tl_internal.cuh"
 
 #include <cuda_fp16.h>
 
 namespace tl {
 namespace {
-
-__device__ __forceinline__ void bfly(float& a, float& b) {
-  const float s = __fadd_rn(a, b);
-  const float d = __fsub_rn(a, b);
-  a = s;
-  b = d;
-}
 
 template <int XQ_DTYPE>
 __global__ void __launch_bounds__(1024)
@@ -41,72 +31,7 @@ rotate_quant_kernel(const uint16_t* __restrict__ x, int K, const int8_t* __restr
   pdl_launch_dependents();
 
   float v[4][8];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int i0 = 256 * j + 8 * lane;
-    const uint4 raw = *reinterpret_cast<const uint4*>(x + base + i0);
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const uint32_t bits = (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
-      v[j][e] = __uint_as_float(bits << 16);
-    }
-    if (signs != nullptr) {
-      const uint2 sraw = *reinterpret_cast<const uint2*>(signs + blk * kBlock + i0);
-      const uint32_t sw[2] = {sraw.x, sraw.y};
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int8_t sg = static_cast<int8_t>((sw[e >> 2] >> (8 * (e & 3))) & 0xFFu);
-        if (sg < 0) v[j][e] = -v[j][e];
-      }
-    }
-  }
-
-  // strides 1, 2, 4: element bits 0..2
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-#pragma unroll
-    for (int h = 1; h < 8; h <<= 1) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        if ((e & h) == 0) bfly(v[j][e], v[j][e + h]);
-      }
-    }
-  }
-  // strides 8, 16, 32, 64, 128: lane bits 0..4
-#pragma unroll
-  for (int t = 1; t < 32; t <<= 1) {
-    const bool upper = (lane & t) != 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float o = __shfl_xor_sync(0xffffffffu, v[j][e], t);
-        v[j][e] = upper ? __fsub_rn(o, v[j][e]) : __fadd_rn(v[j][e], o);
-      }
-    }
-  }
-  // strides 256, 512: j bits 0..1
-#pragma unroll
-  for (int h = 1; h < 4; h <<= 1) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if ((j & h) == 0) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) bfly(v[j][e], v[j + h][e]);
-      }
-    }
-  }
-
-  float amax = 0.f;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      v[j][e] = __fmul_rn(v[j][e], 0.03125f);
-      amax = fmaxf(amax, fabsf(v[j][e]));
-    }
-  }
+  float amax = rotate_block_warp(x + base, signs == nullptr ? nullptr : signs + blk * kBlock, lane, v);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   if (lane == 0) warp_max[blk] = amax;
@@ -122,8 +47,7 @@ rotate_quant_kernel(const uint16_t* __restrict__ x, int K, const int8_t* __restr
     int q[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      int t = __float2int_rn(__fmul_rn(v[j][e], inv));
-      q[e] = max(-127, min(127, t));
+      q[e] = quant_i8(v[j][e], inv);
     }
     const size_t off = base + 256 * j + 8 * lane;
     if (XQ_DTYPE == TL_I8) {

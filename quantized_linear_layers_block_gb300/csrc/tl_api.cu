@@ -170,6 +170,22 @@ int tl_linear_decode(const uint8_t* packed, const int8_t* qT, const float* sw, c
              : TL_ECUDA;
 }
 
+int tl_linear_decode_fused(const uint8_t* packed, const int8_t* qT, const float* sw,
+                           const uint16_t* x, const int8_t* signs, int M, int N, int K, void* y,
+                           int y_dtype, int32_t* acc_dbg, int8_t* xq_out, float* sx_out,
+                           void* stream) {
+  int r = check_linear(packed, qT, sw, x, sw, M, N, K, y, y_dtype, acc_dbg);
+  if (r != TL_OK) return r;
+  if (M > 1 || K > tl::kMaxFusedDecodeK) return TL_EUNSUPPORTED;
+  if (M == 0 || N == 0) return TL_OK;
+  if ((signs && !aligned16(signs)) || (xq_out && !aligned16(xq_out)) || (sx_out && !aligned16(sx_out)))
+    return TL_EINVAL;
+  return tl::launch_decode_fused(reinterpret_cast<const uint32_t*>(packed), qT, sw, x, signs, N, K,
+                                 y, y_dtype, acc_dbg, xq_out, sx_out, as_stream(stream)) == cudaSuccess
+             ? TL_OK
+             : TL_ECUDA;
+}
+
 int tl_get_status(void* stream) {
   int* status = nullptr;
   int r = status_ptr(&status);

@@ -56,6 +56,12 @@ cudaError_t launch_rotate_quant(const uint16_t* x, int M, int K, const int8_t* s
 cudaError_t launch_decode(const uint32_t* packed, const int8_t* qT, const float* sw,
                           const int8_t* xq, const float* sx, int M, int N, int K, void* y,
                           int y_dtype, int32_t* acc_dbg, cudaStream_t st);
+// M = 1 decode with the rotation and quantisation of x done in each CTA (K <= 8192).
+cudaError_t launch_decode_fused(const uint32_t* packed, const int8_t* qT, const float* sw,
+                                const uint16_t* x, const int8_t* signs, int N, int K, void* y,
+                                int y_dtype, int32_t* acc_dbg, int8_t* xq_out, float* sx_out,
+                                cudaStream_t st);
+constexpr int kMaxFusedDecodeK = 8192;
 size_t prefill_workspace_bytes(int M, int N, int K, int num_sms);
 // Returns TL_OK or a tl_status; *cerr receives the CUDA error when TL_ECUDA.
 int launch_prefill(const PrefillArgs& a, int* status, cudaStream_t st, cudaError_t* cerr);
@@ -286,6 +292,93 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
          | (0u << 7) | (0u << 10)                    // A, B format: f16
          | (static_cast<uint32_t>(n >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(m >> 4) << 24);    // M / 16
+}
+
+// ---- input-side rotation of one 1024-column block by one warp
+// Lane l holds the 32 elements i = 256 j + 8 l + e (j = 0..3, e = 0..7),
+// loaded as four coalesced 16-byte vectors. Butterfly strides 1, 2, 4 act on e
+// (registers), 8..128 on the lane index (warp shuffles), 256 and 512 on j
+// (registers): the stages run in the order 1, 2, 4, ..., 512, each butterfly
+// one fp32 add and one subtract, then the exact 1/32 scale. Returns the lane's
+// largest |value|.
+__device__ __forceinline__ void fwht_bfly(float& a, float& b) {
+  const float s = __fadd_rn(a, b);
+  const float d = __fsub_rn(a, b);
+  a = s;
+  b = d;
+}
+
+__device__ __forceinline__ float rotate_block_warp(const uint16_t* __restrict__ xb,
+                                                   const int8_t* __restrict__ sb, int lane,
+                                                   float (&v)[4][8]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i0 = 256 * j + 8 * lane;
+    const uint4 raw = *reinterpret_cast<const uint4*>(xb + i0);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t bits = (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+      v[j][e] = __uint_as_float(bits << 16);
+    }
+    if (sb != nullptr) {
+      const uint2 sraw = *reinterpret_cast<const uint2*>(sb + i0);
+      const uint32_t sg[2] = {sraw.x, sraw.y};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int8_t sgn = static_cast<int8_t>((sg[e >> 2] >> (8 * (e & 3))) & 0xFFu);
+        if (sgn < 0) v[j][e] = -v[j][e];
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if ((e & h) == 0) fwht_bfly(v[j][e], v[j][e + h]);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 1; t < 32; t <<= 1) {
+    const bool upper = (lane & t) != 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float o = __shfl_xor_sync(0xffffffffu, v[j][e], t);
+        v[j][e] = upper ? __fsub_rn(o, v[j][e]) : __fadd_rn(v[j][e], o);
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 1; h < 4; h <<= 1) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if ((j & h) == 0) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) fwht_bfly(v[j][e], v[j + h][e]);
+      }
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      v[j][e] = __fmul_rn(v[j][e], 0.03125f);
+      amax = fmaxf(amax, fabsf(v[j][e]));
+    }
+  }
+  return amax;
+}
+
+// Symmetric int8 code of one rotated value: clamp(rne(fl32(v inv)), -127, 127).
+__device__ __forceinline__ int quant_i8(float v, float inv) {
+  const int t = __float2int_rn(__fmul_rn(v, inv));
+  return max(-127, min(127, t));
 }
 
 }  // namespace tl

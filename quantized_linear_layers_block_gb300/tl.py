@@ -20,6 +20,7 @@ _lock = threading.Lock()
 
 TL_OK, TL_EINVAL, TL_EUNSUPPORTED, TL_ECUDA, TL_ETIMEOUT, TL_EDATA, TL_ENOSPACE = range(7)
 TL_I8, TL_F16, TL_BF16, TL_F32 = 1, 2, 3, 4
+FUSED_DECODE_MAX_K = 8192
 
 # name -> (restype, argtypes)
 _P = ctypes.c_void_p
@@ -36,6 +37,7 @@ SIGNATURES = {
     "tl_linear_prefill": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P, _SZ, _P]),
     "tl_linear_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P]),
     "tl_linear_prefill_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P]),
+    "tl_linear_decode_fused": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P, _P, _P]),
     "tl_get_status": (_I, [_P]),
 }
 
@@ -196,6 +198,20 @@ def tl_linear_decode(packed, qT, sw, xq, sx, N: int, K: int, y_dtype: int = TL_B
     return y
 
 
+def tl_linear_decode_fused(packed, qT, sw, x, N: int, K: int, y_dtype: int = TL_BF16,
+                           signs=None, y: torch.Tensor | None = None,
+                           acc_dbg: torch.Tensor | None = None, xq_out: torch.Tensor | None = None,
+                           sx_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One token (x bf16 [1,K]) through rotation, quantisation and the decode GEMV in one launch."""
+    _dev_tensor(x, torch.bfloat16, "x")
+    M = x.shape[0]
+    y = _linear_out(M, N, y_dtype, x.device, y)
+    _check(lib().tl_linear_decode_fused(_ptr(packed), _ptr(qT), _ptr(sw), _ptr(x), _ptr(signs), M, N, K,
+                                        _ptr(y), y_dtype, _ptr(acc_dbg), _ptr(xq_out), _ptr(sx_out),
+                                        _stream(stream)), "tl_linear_decode_fused")
+    return y
+
+
 def tl_get_status(stream=None) -> int:
     return lib().tl_get_status(_stream(stream))
 
@@ -205,8 +221,9 @@ class TernaryLinear:
 
     Built once from int8 codes [N,K] and fp16 group scales [N,K/128]; forward()
     takes bf16 activations [M,K] on the host or the device and returns y [M,N]
-    where it found x. M <= 32 runs the decode kernel, larger M the tensor-core
-    prefill kernel; both give the same integer accumulator and the same y.
+    where it found x. M = 1 runs the fused rotate+quantise+decode kernel (K <= 8192),
+    M <= 32 the decode kernel, larger M the tensor-core prefill kernel; all give
+    the same integer accumulator and the same y.
     """
 
     DECODE_MAX_M = 32

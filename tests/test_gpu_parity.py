@@ -190,6 +190,40 @@ def test_decode_m1_shapes(tl, K):
     _compare(L, acc, y, 4)
 
 
+@pytest.mark.parametrize("K", [1024, 2048, 3072, 5120, 6144, 7168, 8192])
+@pytest.mark.parametrize("signed", [False, True], ids=["plain", "signs"])
+def test_decode_fused_matches_two_step(tl, K, signed):
+    """One launch (rotate + quantise + decode) equals the two-kernel path bit for bit."""
+    L = synth.config_inputs("decode", M=1, N=256, K=K)
+    packed, qT, sw = pack_dev(tl, L)
+    x = x_dev(L)
+    signs = None
+    if signed:
+        signs = dev(np.where(np.random.default_rng(K).random(K) < 0.5, -1, 1).astype(np.int8))
+    acc2 = torch.empty((1, L.N), dtype=torch.int32, device="cuda")
+    xq, sx = tl.tl_rotate_quant_act(x, signs=signs, xq_dtype=tl.TL_I8)
+    y2 = tl.tl_linear_decode(packed, qT, sw, xq, sx, L.N, L.K, 4, acc_dbg=acc2)
+    acc1 = torch.full((1, L.N), ACC_SENTINEL, dtype=torch.int32, device="cuda")
+    xq1 = torch.zeros((1, K), dtype=torch.int8, device="cuda")
+    sx1 = torch.zeros((1,), dtype=torch.float32, device="cuda")
+    y1 = tl.tl_linear_decode_fused(packed, qT, sw, x, L.N, L.K, 4, signs=signs, acc_dbg=acc1,
+                                   xq_out=xq1, sx_out=sx1)
+    check_status(tl)
+    assert torch.equal(xq1, xq) and torch.equal(sx1, sx)
+    assert torch.equal(acc1, acc2) and torch.equal(y1, y2)
+    if not signed:
+        _compare(L, acc1.cpu().numpy(), y1, 4)
+
+
+def test_decode_fused_full_size(tl):
+    L = synth.config_inputs("decode")
+    packed, qT, sw = pack_dev(tl, L)
+    acc = torch.full((1, L.N), ACC_SENTINEL, dtype=torch.int32, device="cuda")
+    y = tl.tl_linear_decode_fused(packed, qT, sw, x_dev(L), L.N, L.K, 3, acc_dbg=acc)
+    check_status(tl)
+    _compare(L, acc.cpu().numpy(), y, 3, rows=_sample_rows(L.N))
+
+
 @pytest.mark.parametrize("M,K", [(2, 17408), (7, 17408), (16, 17408), (32, 17408), (32, 1024)])
 def test_decode_slabs(tl, M, K):
     """M * K beyond one shared-memory slab: K is processed in slabs with partial sums."""
