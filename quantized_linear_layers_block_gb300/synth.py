@@ -143,6 +143,26 @@ CONFIGS = {
 
 SWEEP_M = (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 4096)
 
+# The int8 128-group codec's payload: one bf16 part per rank of the row-parallel
+# all-reduce of the 5120-wide hidden state (P1 §6: 256 tokens, 2.6 MB; P3 §5:
+# 1584-row payloads). Each part is N(0,1) with the same few outlier channels
+# (0.2 % of H, scaled by 20) in every part, rounded to bf16.
+CODEC = dict(R=1584, H=5120, parts=2, outlier_frac=0.002, outlier_factor=20.0, seed=6000)
+
+
+def codec_parts(seed: int, R: int, H: int, parts: int, outlier_frac: float = 0.002,
+                outlier_factor: float = 20.0) -> list:
+    """bf16 bits [R, H] for each of `parts` ranks; the outlier channels are drawn first."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    n_out = int(round(outlier_frac * H))
+    ch = rng.choice(H, size=n_out, replace=False) if n_out > 0 else np.zeros(0, dtype=np.int64)
+    out = []
+    for _ in range(parts):
+        x = rng.standard_normal((R, H), dtype=np.float32)
+        x[:, ch] *= np.float32(outlier_factor)
+        out.append(bf16_bits_from_f32(x))
+    return out
+
 
 def config_seed(name: str, layer: int = 0) -> int:
     cfg = CONFIGS[name]["cfg"]
@@ -208,3 +228,20 @@ def torch_config_layer(name: str, layer: int, M: int | None = None, device: str 
     if M is not None:
         c["M"] = M
     return torch_layer(config_seed(name, layer), device=device, **c)
+
+
+def torch_codec_parts(seed: int, R: int, H: int, parts: int, outlier_frac: float = 0.002,
+                      outlier_factor: float = 20.0, device: str = "cuda") -> list:
+    """Device-side draws of the codec payload (same recipe, torch's generator), bf16 tensors."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    n_out = int(round(outlier_frac * H))
+    ch = torch.randperm(H, generator=g, device=device)[:n_out]
+    out = []
+    for _ in range(parts):
+        x = torch.randn((R, H), generator=g, device=device, dtype=torch.float32)
+        x[:, ch] *= outlier_factor
+        out.append(x.to(torch.bfloat16))
+    return out
+
