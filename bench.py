@@ -376,6 +376,9 @@ def main(argv=None):
     if status != tl.TL_OK:
         raise RuntimeError(f"device status after timing: {tl.tl_strerror(status)}")
 
+    # ---------------- int8 128-group codec (compress, decompress-and-add), 1584 x 5120
+    codec = codec_bench(dev, stream, max(4, args.warmup), max(8, K))
+
     # ---------------- end to end through TernaryLinear.forward with pinned host buffers
     e2e_steps = 0 if args.no_e2e else max(1, min(K, 8))
     e2e_dsteps = 0 if args.no_e2e else max(1, min(Kd, 64))
@@ -434,6 +437,7 @@ def main(argv=None):
         "e2e": {"value": ws * e2e_steps * LAYERS * flop_layer / e2e_pre_s / 1e12, "unit": "TOPS",
                 "h2d_bytes_per_step": LAYERS * P["M"] * P["K"] * 2,
                 "d2h_bytes_per_step": LAYERS * P["M"] * P["N"] * 2},
+        "codec": codec,
         "gpu_launches": K * LAYERS * 2 + Kd * LAYERS * 2,
         "clocks": clk,
     }
@@ -449,6 +453,56 @@ def main(argv=None):
     if ws > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def codec_bench(dev, stream, warmup: int, reps: int) -> dict:
+    """Times tl_codec_quant and tl_codec_dequant_add (one peer) on the 1584 x 5120
+    payload, rotating over 16 payload buffers (260 MB of bf16, larger than L2)."""
+    import torch
+    from quantized_linear_layers_block_gb300 import synth, tl
+    c = synth.CODEC
+    R, H, nb = c["R"], c["H"], 16
+    own = synth.torch_codec_parts(c["seed"], R, H, nb, c["outlier_frac"], c["outlier_factor"], device=str(dev))
+    q = [torch.empty((1, R, H), dtype=torch.int8, device=dev) for _ in range(nb)]
+    sc = [torch.empty((1, R, H // 128), dtype=torch.float32, device=dev) for _ in range(nb)]
+    out = [torch.empty((R, H), dtype=torch.bfloat16, device=dev) for _ in range(nb)]
+
+    def run_quant(i):
+        tl.tl_codec_quant(own[i], q=q[i][0], scale=sc[i][0])
+
+    def run_dq(i):
+        tl.tl_codec_dequant_add(own[i], q[(i + 1) % nb], sc[(i + 1) % nb], out=out[i])
+
+    res = {}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    bytes_q = 2 * R * H + R * H + 4 * R * (H // 128)
+    bytes_dq = 2 * R * H + R * H + 4 * R * (H // 128) + 2 * R * H
+    peaks, _ = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    for name, fn, nbytes in (("quant", run_quant, bytes_q), ("dequant_add", run_dq, bytes_dq)):
+        for i in range(nb):          # resolve attributes before capture
+            fn(i)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()   # one graph of nb launches: no host launch cost inside
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            for i in range(nb):
+                fn(i)
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = 1e3 * e0.elapsed_time(e1) / (reps * nb)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        res[name] = {"us": us, "GB/s": gbs, "bytes": nbytes, "frac_hbm": gbs / hbm}
+    if tl.tl_get_status() != tl.TL_OK:
+        raise RuntimeError("device status after the codec timing")
+    res["workload"] = f"R={R} H={H} bf16, one peer; 16 payload buffers (larger than L2)"
+    res["launches"] = 2 * nb * (reps + warmup + 2)
+    return res
 
 
 def _profiled_traffic() -> dict:

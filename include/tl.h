@@ -196,6 +196,38 @@ int tl_linear_prefill_noalloc(const uint8_t* packed, const int8_t* qT, const flo
                               void* y, int y_dtype, int32_t* acc_dbg, void* stream);
 
 /*
+ * int8 128-group codec of a row-parallel all-reduce payload (Qiita item
+ * ecc183fae033565af7cb §6 "最後に残った問題": int8 with one scale per 128
+ * elements, all-gathered, each rank adding its own part in bf16; item
+ * 66e136acefd5a54b2f1d §5 "解説: 長文を読む速度(prefill)": "compress" and
+ * "decompress and add" as one kernel each). The all-gather between the two
+ * calls belongs to the caller.
+ *
+ * tl_codec_quant compresses one part:
+ *   x      in  bf16 bit patterns [R, H], row-major; H a multiple of 128
+ *   q      out int8 [R, H]
+ *   scale  out fp32 [R, H/128]
+ * Per 128-element group: a = max |x|; inv = fl32(127/a);
+ * q = clamp(rne(fl32(x inv)), -127, 127); scale = fl32(a/127); a = 0 gives
+ * q = 0 and scale = 0.
+ *
+ * tl_codec_dequant_add decompresses the peers' parts and adds them to the own:
+ *   own          in  bf16 [R, H], the rank's own part (not compressed)
+ *   q_peers      in  int8 [npeers, R, H]; scale_peers fp32 [npeers, R, H/128]
+ *   npeers       0..7 (more returns TL_EUNSUPPORTED; 0 copies own to out)
+ *   out          out bf16 [R, H]; may be the same buffer as own
+ * out = rne_bf16(((own + fl32(q_0 scale_0)) + fl32(q_1 scale_1)) + ...), every
+ * product and sum an fp32 operation.
+ *
+ * Pointers are device pointers, 16-byte aligned; R = 0 is a no-op; H not a
+ * multiple of 128 returns TL_EUNSUPPORTED; NULL, misaligned or negative
+ * arguments return TL_EINVAL. Nothing is launched on an error.
+ */
+int tl_codec_quant(const uint16_t* x, int R, int H, int8_t* q, float* scale, void* stream);
+int tl_codec_dequant_add(const uint16_t* own, const int8_t* q_peers, const float* scale_peers,
+                         int npeers, int R, int H, uint16_t* out, void* stream);
+
+/*
  * Synchronises `stream`, then returns and clears the current device's status
  * word: TL_OK, TL_ETIMEOUT or TL_EDATA (first error recorded), or TL_ECUDA if
  * the synchronisation itself failed.

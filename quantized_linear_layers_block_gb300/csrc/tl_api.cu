@@ -186,6 +186,30 @@ int tl_linear_decode_fused(const uint8_t* packed, const int8_t* qT, const float*
              : TL_ECUDA;
 }
 
+int tl_codec_quant(const uint16_t* x, int R, int H, int8_t* q, float* scale, void* stream) {
+  if (R < 0 || H <= 0) return TL_EINVAL;
+  if (H % tl::kGroup != 0) return TL_EUNSUPPORTED;
+  if (R == 0) return TL_OK;
+  if (!x || !q || !scale) return TL_EINVAL;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(scale)) return TL_EINVAL;
+  return tl::launch_codec_quant(x, R, H, q, scale, as_stream(stream)) == cudaSuccess ? TL_OK
+                                                                                      : TL_ECUDA;
+}
+
+int tl_codec_dequant_add(const uint16_t* own, const int8_t* q_peers, const float* scale_peers,
+                         int npeers, int R, int H, uint16_t* out, void* stream) {
+  if (R < 0 || H <= 0 || npeers < 0) return TL_EINVAL;
+  if (H % tl::kGroup != 0 || npeers > tl::kMaxCodecPeers) return TL_EUNSUPPORTED;
+  if (R == 0) return TL_OK;
+  if (!own || !out || (npeers > 0 && (!q_peers || !scale_peers))) return TL_EINVAL;
+  if (!aligned16(own) || !aligned16(out) || (npeers > 0 && (!aligned16(q_peers) || !aligned16(scale_peers))))
+    return TL_EINVAL;
+  return tl::launch_codec_dequant_add(own, q_peers, scale_peers, npeers, R, H, out,
+                                      as_stream(stream)) == cudaSuccess
+             ? TL_OK
+             : TL_ECUDA;
+}
+
 int tl_get_status(void* stream) {
   int* status = nullptr;
   int r = status_ptr(&status);

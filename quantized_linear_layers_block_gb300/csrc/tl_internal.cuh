@@ -62,6 +62,11 @@ cudaError_t launch_decode_fused(const uint32_t* packed, const int8_t* qT, const 
                                 int y_dtype, int32_t* acc_dbg, int8_t* xq_out, float* sx_out,
                                 cudaStream_t st);
 constexpr int kMaxFusedDecodeK = 8192;
+constexpr int kMaxCodecPeers = 7;
+cudaError_t launch_codec_quant(const uint16_t* x, int R, int H, int8_t* q, float* scale,
+                               cudaStream_t st);
+cudaError_t launch_codec_dequant_add(const uint16_t* own, const int8_t* q, const float* scale,
+                                     int npeers, int R, int H, uint16_t* out, cudaStream_t st);
 size_t prefill_workspace_bytes(int M, int N, int K, int num_sms);
 // Returns TL_OK or a tl_status; *cerr receives the CUDA error when TL_ECUDA.
 int launch_prefill(const PrefillArgs& a, int* status, cudaStream_t st, cudaError_t* cerr);

@@ -38,6 +38,8 @@ SIGNATURES = {
     "tl_linear_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P]),
     "tl_linear_prefill_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P]),
     "tl_linear_decode_fused": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P, _P, _P]),
+    "tl_codec_quant": (_I, [_P, _I, _I, _P, _P, _P]),
+    "tl_codec_dequant_add": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "tl_get_status": (_I, [_P]),
 }
 
@@ -212,6 +214,36 @@ def tl_linear_decode_fused(packed, qT, sw, x, N: int, K: int, y_dtype: int = TL_
     return y
 
 
+def tl_codec_quant(x: torch.Tensor, q: torch.Tensor | None = None, scale: torch.Tensor | None = None,
+                   stream=None):
+    """Compress a bf16 payload [R,H] -> (int8 q [R,H], fp32 scale [R,H/128])."""
+    _dev_tensor(x, torch.bfloat16, "x")
+    R, H = x.shape
+    if q is None:
+        q = torch.empty((R, H), dtype=torch.int8, device=x.device)
+    if scale is None:
+        scale = torch.empty((R, H // 128), dtype=torch.float32, device=x.device)
+    _check(lib().tl_codec_quant(_ptr(x), R, H, _ptr(q), _ptr(scale), _stream(stream)), "tl_codec_quant")
+    return q, scale
+
+
+def tl_codec_dequant_add(own: torch.Tensor, q_peers: torch.Tensor | None, scale_peers: torch.Tensor | None,
+                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """own bf16 [R,H] + the peers' decompressed parts (q int8 [P,R,H], scale fp32 [P,R,H/128]) -> bf16 [R,H]."""
+    _dev_tensor(own, torch.bfloat16, "own")
+    R, H = own.shape
+    npeers = 0
+    if q_peers is not None:
+        _dev_tensor(q_peers, torch.int8, "q_peers")
+        _dev_tensor(scale_peers, torch.float32, "scale_peers")
+        npeers = q_peers.shape[0] if q_peers.dim() == 3 else 1
+    if out is None:
+        out = torch.empty_like(own)
+    _check(lib().tl_codec_dequant_add(_ptr(own), _ptr(q_peers), _ptr(scale_peers), npeers, R, H, _ptr(out),
+                                      _stream(stream)), "tl_codec_dequant_add")
+    return out
+
+
 def tl_get_status(stream=None) -> int:
     return lib().tl_get_status(_stream(stream))
 
@@ -221,9 +253,9 @@ class TernaryLinear:
 
     Built once from int8 codes [N,K] and fp16 group scales [N,K/128]; forward()
     takes bf16 activations [M,K] on the host or the device and returns y [M,N]
-    where it found x. M = 1 runs the fused rotate+quantise+decode kernel (K <= 8192),
-    M <= 32 the decode kernel, larger M the tensor-core prefill kernel; all give
-    the same integer accumulator and the same y.
+    where it found x. M <= 32 runs rotate+quantise and the decode kernel, larger M
+    rotate+quantise and the tensor-core prefill kernel; both give the same
+    integer accumulator and the same y.
     """
 
     DECODE_MAX_M = 32

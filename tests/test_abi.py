@@ -84,3 +84,22 @@ def test_argument_errors_without_gpu(lib):
     assert lib.tl_rotate_quant_act(None, 0, 2048, None, None, tl.TL_F16, None, None) == tl.TL_OK
     sz = ctypes.c_size_t(99)
     assert lib.tl_prefill_workspace_size(0, 128, 1024, ctypes.byref(sz)) == tl.TL_OK and sz.value == 0
+
+
+def test_codec_argument_errors_without_gpu(lib):
+    from quantized_linear_layers_block_gb300 import tl
+    P = ctypes.c_void_p
+    bad = P(16 + 4)
+    ok = P(4096)
+    assert lib.tl_codec_quant(ok, 4, 200, ok, ok, None) == tl.TL_EUNSUPPORTED
+    assert lib.tl_codec_quant(ok, -1, 256, ok, ok, None) == tl.TL_EINVAL
+    assert lib.tl_codec_quant(ok, 4, 0, ok, ok, None) == tl.TL_EINVAL
+    assert lib.tl_codec_quant(ok, 4, 256, None, ok, None) == tl.TL_EINVAL
+    assert lib.tl_codec_quant(ok, 4, 256, ok, bad, None) == tl.TL_EINVAL
+    assert lib.tl_codec_quant(None, 0, 256, None, None, None) == tl.TL_OK
+    assert lib.tl_codec_dequant_add(ok, ok, ok, 8, 4, 256, ok, None) == tl.TL_EUNSUPPORTED
+    assert lib.tl_codec_dequant_add(ok, ok, ok, -1, 4, 256, ok, None) == tl.TL_EINVAL
+    assert lib.tl_codec_dequant_add(ok, ok, ok, 1, 4, 384 + 64, ok, None) == tl.TL_EUNSUPPORTED
+    assert lib.tl_codec_dequant_add(ok, None, ok, 1, 4, 256, ok, None) == tl.TL_EINVAL
+    assert lib.tl_codec_dequant_add(ok, ok, ok, 1, 4, 256, bad, None) == tl.TL_EINVAL
+    assert lib.tl_codec_dequant_add(None, None, None, 1, 0, 256, None, None) == tl.TL_OK

@@ -202,3 +202,15 @@ def test_planted_mistake_is_caught(monkeypatch, name, fake):
         except (AssertionError, ValueError, IndexError):
             caught.append(pin.__name__)
     assert caught, f"no pin caught the planted mistake in {name}"
+
+
+def test_tiny_group_overflowing_inverse():
+    """A group of bf16 subnormals: inv = 127/a overflows to +inf; non-zeros code to
+    +-127 (x inf = +-inf, clamped) and exact zeros to 0."""
+    x = np.zeros((1, 128), dtype=np.uint16)
+    x[0, 3] = 0x0001          # +9.2e-41
+    x[0, 7] = 0x8002          # -1.8e-40
+    q, s = C.quantize_groups(x)
+    assert s[0, 0] > 0 and np.isfinite(s[0, 0])
+    assert q[0, 3] == 127 and q[0, 7] == -127
+    assert np.count_nonzero(q) == 2
