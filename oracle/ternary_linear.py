@@ -271,3 +271,37 @@ def rel_fro(y: np.ndarray, ref: np.ndarray) -> float:
     """Relative Frobenius error ||y - ref||_F / ||ref||_F."""
     ref = np.asarray(ref, dtype=np.float64)
     return float(np.linalg.norm(np.asarray(y, dtype=np.float64) - ref) / np.linalg.norm(ref))
+
+
+# --------------------------------------------------------------------------
+# Float-activation decode (P1 §5): the same ternary layer without activation
+# quantisation, accumulated in floating point.
+# --------------------------------------------------------------------------
+
+def layer_float_act(x_bits, codes, s, signs=None, rows: np.ndarray | None = None) -> dict:
+    """y[m,n] = sum_g s[n,g] sum_{k in g} code[n,k] xr[m,k] with xr the fp32
+    rotation (bit-identical to the library's) and s the fp16 group scales.
+
+    P1 §5 "効かなかったもの" contrasts the int8 dp4a decode GEMV with the
+    production decode, which keeps the activations in floating point and was
+    the more accurate of the two. Reading: the rotated activations stay fp32,
+    the weights are code * s with the original fp16 scales (no int8 q), and
+    the result is the plain definition evaluated in fp64 (every product is
+    exact in fp64; the sums carry fp64 rounding only, far below the fp32
+    tolerance a GPU evaluation is held to).
+
+    Returns y64 [M,N] (fp64) and T [M,N] = sum_g |s| sum_k |code xr|, the sum
+    of the absolute terms that bounds the rounding error of any fp32
+    evaluation order.
+    """
+    xr = rotate_fp32(x_bits, signs).astype(np.float64)
+    c = np.asarray(codes, dtype=np.float64)
+    sf = np.asarray(s, dtype=np.float16).astype(np.float64)
+    if rows is not None:
+        c = c[rows]
+        sf = sf[rows]
+    N, K = c.shape
+    W = c * np.repeat(sf, GROUP, axis=1)[:, :K]
+    y64 = xr @ W.T
+    T = np.abs(xr) @ np.abs(W).T
+    return dict(xr=xr.astype(np.float32), y64=y64, T=T)
