@@ -252,6 +252,7 @@ def main(argv=None):
     # ---------------- inputs: 64 layer buffers per workload, resident in HBM
     P, D = PREFILL, DECODE
     pre_layers, dec_layers = [], []
+    dec_scales = []
     for li in range(LAYERS):
         codes, s, x = synth.torch_config_layer(P["name"], li, device=str(dev))
         lay = tl.TernaryLinear(codes, s, device=dev)
@@ -259,8 +260,9 @@ def main(argv=None):
         pre_layers.append((lay, x, torch.empty((P["M"], P["N"]), dtype=torch.bfloat16, device=dev)))
         codes, s, x = synth.torch_config_layer(D["name"], li, device=str(dev))
         lay = tl.TernaryLinear(codes, s, device=dev)
-        del codes, s
+        del codes
         dec_layers.append((lay, x, torch.empty((D["M"], D["N"]), dtype=torch.bfloat16, device=dev)))
+        dec_scales.append(s.contiguous())
     torch.cuda.synchronize()
     if tl.tl_get_status() != tl.TL_OK:
         raise RuntimeError("device status after packing")
@@ -268,6 +270,7 @@ def main(argv=None):
     xq_p = torch.empty((P["M"], P["K"]), dtype=torch.float16, device=dev)
     sx_p = torch.empty((P["M"],), dtype=torch.float32, device=dev)
     xq_d = torch.empty((D["M"], D["K"]), dtype=torch.int8, device=dev)
+    xr_d = torch.empty((D["M"], D["K"]), dtype=torch.float32, device=dev)
     sx_d = torch.empty((D["M"],), dtype=torch.float32, device=dev)
     ws_p = pre_layers[0][0]._workspace(P["M"])
     stream = torch.cuda.current_stream(dev)
@@ -292,6 +295,15 @@ def main(argv=None):
         lay, _, y = dec_layers[li]
         tl.tl_linear_decode(lay.packed, lay.qT, lay.sw, xq_d, sx_d, D["N"], D["K"], tl.TL_BF16, y=y)
 
+    def decode_f32act(li):
+        lay, x, y = dec_layers[li]
+        tl.tl_rotate_act(x, xr=xr_d)
+        tl.tl_linear_decode_f32act(lay.packed, dec_scales[li], xr_d, D["N"], D["K"], tl.TL_BF16, y=y)
+
+    def decode_f32act_kernel(li):
+        lay, _, y = dec_layers[li]
+        tl.tl_linear_decode_f32act(lay.packed, dec_scales[li], xr_d, D["N"], D["K"], tl.TL_BF16, y=y)
+
     def decode_fused(li):
         lay, x, y = dec_layers[li]
         tl.tl_linear_decode_fused(lay.packed, lay.qT, lay.sw, x, D["N"], D["K"], tl.TL_BF16, y=y)
@@ -306,6 +318,17 @@ def main(argv=None):
     g_dec = torch.cuda.CUDAGraph()
     g_dk = torch.cuda.CUDAGraph()
     g_df = torch.cuda.CUDAGraph()
+    g_ff = torch.cuda.CUDAGraph()
+    g_fk = torch.cuda.CUDAGraph()
+    for li in range(LAYERS):          # resolve the float decode's kernel attributes before capture
+        decode_f32act(li)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g_ff, capture_error_mode="relaxed"):
+        for li in range(LAYERS):
+            decode_f32act(li)
+    with torch.cuda.graph(g_fk, capture_error_mode="relaxed"):
+        for li in range(LAYERS):
+            decode_f32act_kernel(li)
     with torch.cuda.graph(g_dec, capture_error_mode="relaxed"):
         for li in range(LAYERS):
             decode_layer(li)
@@ -319,6 +342,8 @@ def main(argv=None):
         g_dec.replay()
         g_dk.replay()
         g_df.replay()
+        g_ff.replay()
+        g_fk.replay()
     torch.cuda.synchronize()
     if tl.tl_get_status() != tl.TL_OK:
         raise RuntimeError("device status after warm-up")
@@ -372,6 +397,8 @@ def main(argv=None):
     reps = max(8, Kd // 4)
     k2_ms = graph_us(g_dk, reps) * 1e-3
     fused_us = graph_us(g_df, reps)
+    f32_layer_us = graph_us(g_ff, reps)
+    f32_kernel_us = graph_us(g_fk, reps)
     status = tl.tl_get_status()
     if status != tl.TL_OK:
         raise RuntimeError(f"device status after timing: {tl.tl_strerror(status)}")
@@ -437,6 +464,15 @@ def main(argv=None):
         "e2e": {"value": ws * e2e_steps * LAYERS * flop_layer / e2e_pre_s / 1e12, "unit": "TOPS",
                 "h2d_bytes_per_step": LAYERS * P["M"] * P["K"] * 2,
                 "d2h_bytes_per_step": LAYERS * P["M"] * P["N"] * 2},
+        "decode_f32act": {
+            "metric": "float-activation decode GEMV weight-stream GB/s @M=1",
+            "layer_us": f32_layer_us, "kernel_us": f32_kernel_us,
+            "value": wb / (f32_layer_us * 1e-6) / 1e9, "unit": "GB/s",
+            "kernel_GB/s": (wb + 2 * D["N"] * (D["K"] // 128) + 4 * D["K"]) / (f32_kernel_us * 1e-6) / 1e9,
+            "bound": "alu",
+            "note": "rotation (fp32) then the fp32 GEMV from packed codes and fp16 scales; "
+                    "64 layer buffers in a CUDA graph",
+        },
         "codec": codec,
         "gpu_launches": K * LAYERS * 2 + Kd * LAYERS * 2,
         "clocks": clk,

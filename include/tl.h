@@ -196,6 +196,36 @@ int tl_linear_prefill_noalloc(const uint8_t* packed, const int8_t* qT, const flo
                               void* y, int y_dtype, int32_t* acc_dbg, void* stream);
 
 /*
+ * The input-side rotation alone, fp32 out: xr = (1/32) H1024 (signs * x) per
+ * 1024-block of each token, the same arithmetic as tl_rotate_quant_act's
+ * first step (bit for bit).
+ *   x      in  bf16 bit patterns [M, K]; K a multiple of 1024, K <= 32768
+ *   signs  in  optional int8 [K] of +1/-1 (NULL: none)
+ *   xr     out fp32 [M, K]
+ */
+int tl_rotate_act(const uint16_t* x, int M, int K, const int8_t* signs, float* xr, void* stream);
+
+/*
+ * Decode (1 <= M <= 4) with floating-point activations (Qiita item
+ * ecc183fae033565af7cb §5 "効かなかったもの": the production decode kept the
+ * activations in floating point and was more exact than the int8 GEMV):
+ *   y[m,n] = sum_g s[n,g] sum_{k in g} code[n,k] xr[m,k]
+ * in fp32 arithmetic from the packed codes and the ORIGINAL fp16 group scales;
+ * no activation quantisation and no int8 q. Same weights as the int8 path
+ * (packed from tl_pack_weights) plus s.
+ *   packed  in  uint8 [N, K/4] (tl_pack_weights)
+ *   s       in  fp16 bit patterns [N, K/128], the scales given to tl_pack_weights
+ *   xr      in  fp32 [M, K] (tl_rotate_act)
+ *   y       out [M, N], y_dtype TL_F32 or TL_BF16 (rne of the fp32 sum)
+ * M > 4 or M * K > 36864 returns TL_EUNSUPPORTED (the activations are staged
+ * in shared memory). The sum is in fp32 in an order of the kernel's own; every
+ * product code * xr is exact (for |xr| >= 2^-112), so the error is that of
+ * at most K/1024 + 23 roundings per term.
+ */
+int tl_linear_decode_f32act(const uint8_t* packed, const uint16_t* s, const float* xr, int M, int N,
+                            int K, void* y, int y_dtype, void* stream);
+
+/*
  * int8 128-group codec of a row-parallel all-reduce payload (Qiita item
  * ecc183fae033565af7cb §6 "最後に残った問題": int8 with one scale per 128
  * elements, all-gathered, each rank adding its own part in bf16; item

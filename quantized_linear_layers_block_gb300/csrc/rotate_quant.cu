@@ -69,7 +69,31 @@ rotate_quant_kernel(const uint16_t* __restrict__ x, int K, const int8_t* __restr
   }
 }
 
+// The rotation alone, fp32 out (the float-activation decode's input).
+__global__ void __launch_bounds__(1024)
+rotate_kernel(const uint16_t* __restrict__ x, int K, const int8_t* __restrict__ signs,
+              float* __restrict__ xr) {
+  const int lane = threadIdx.x & 31;
+  const int blk = threadIdx.x >> 5;
+  const size_t base = blockIdx.x * static_cast<size_t>(K) + static_cast<size_t>(blk) * kBlock;
+  pdl_wait_prior();
+  pdl_launch_dependents();
+  float v[4][8];
+  rotate_block_warp(x + base, signs == nullptr ? nullptr : signs + blk * kBlock, lane, v);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float4* o = reinterpret_cast<float4*>(xr + base + 256 * j + 8 * lane);
+    o[0] = make_float4(v[j][0], v[j][1], v[j][2], v[j][3]);
+    o[1] = make_float4(v[j][4], v[j][5], v[j][6], v[j][7]);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_rotate(const uint16_t* x, int M, int K, const int8_t* signs, float* xr,
+                          cudaStream_t st) {
+  return launch_pdl(rotate_kernel, dim3(M), dim3((K / kBlock) * 32), 0, st, x, K, signs, xr);
+}
 
 cudaError_t launch_rotate_quant(const uint16_t* x, int M, int K, const int8_t* signs, void* xq,
                                 int xq_dtype, float* sx, cudaStream_t st) {

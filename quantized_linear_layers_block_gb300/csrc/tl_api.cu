@@ -186,6 +186,30 @@ int tl_linear_decode_fused(const uint8_t* packed, const int8_t* qT, const float*
              : TL_ECUDA;
 }
 
+int tl_rotate_act(const uint16_t* x, int M, int K, const int8_t* signs, float* xr, void* stream) {
+  if (M < 0 || K <= 0) return TL_EINVAL;
+  if (K % tl::kBlock != 0 || K > tl::kMaxK) return TL_EUNSUPPORTED;
+  if (M == 0) return TL_OK;
+  if (!x || !xr) return TL_EINVAL;
+  if (!aligned16(x) || !aligned16(xr) || (signs && !aligned16(signs))) return TL_EINVAL;
+  return tl::launch_rotate(x, M, K, signs, xr, as_stream(stream)) == cudaSuccess ? TL_OK : TL_ECUDA;
+}
+
+int tl_linear_decode_f32act(const uint8_t* packed, const uint16_t* s, const float* xr, int M, int N,
+                            int K, void* y, int y_dtype, void* stream) {
+  if (M < 0) return TL_EINVAL;
+  int r = check_nk(N, K);
+  if (r != TL_OK) return r;
+  if (y_dtype != TL_BF16 && y_dtype != TL_F32) return TL_EINVAL;
+  if (M > tl::kMaxF32ActM || static_cast<long long>(M) * K > tl::kMaxF32ActMK) return TL_EUNSUPPORTED;
+  if (M == 0 || N == 0) return TL_OK;
+  if (!packed || !s || !xr || !y) return TL_EINVAL;
+  if (!aligned16(packed) || !aligned16(s) || !aligned16(xr) || !aligned16(y)) return TL_EINVAL;
+  return tl::launch_decode_f32act(packed, s, xr, M, N, K, y, y_dtype, as_stream(stream)) == cudaSuccess
+             ? TL_OK
+             : TL_ECUDA;
+}
+
 int tl_codec_quant(const uint16_t* x, int R, int H, int8_t* q, float* scale, void* stream) {
   if (R < 0 || H <= 0) return TL_EINVAL;
   if (H % tl::kGroup != 0) return TL_EUNSUPPORTED;

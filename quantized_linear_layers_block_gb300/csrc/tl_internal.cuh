@@ -63,6 +63,12 @@ cudaError_t launch_decode_fused(const uint32_t* packed, const int8_t* qT, const 
                                 cudaStream_t st);
 constexpr int kMaxFusedDecodeK = 8192;
 constexpr int kMaxCodecPeers = 7;
+constexpr int kMaxF32ActM = 4;            // tokens of the float-activation decode
+constexpr int kMaxF32ActMK = 36864;       // M * K bound: the staged fp32 activations fit shared memory
+cudaError_t launch_rotate(const uint16_t* x, int M, int K, const int8_t* signs, float* xr,
+                          cudaStream_t st);
+cudaError_t launch_decode_f32act(const uint8_t* packed, const uint16_t* s, const float* xr, int M,
+                                 int N, int K, void* y, int y_dtype, cudaStream_t st);
 cudaError_t launch_codec_quant(const uint16_t* x, int R, int H, int8_t* q, float* scale,
                                cudaStream_t st);
 cudaError_t launch_codec_dequant_add(const uint16_t* own, const int8_t* q, const float* scale,

@@ -38,6 +38,8 @@ SIGNATURES = {
     "tl_linear_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P]),
     "tl_linear_prefill_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P]),
     "tl_linear_decode_fused": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P, _P, _P]),
+    "tl_rotate_act": (_I, [_P, _I, _I, _P, _P, _P]),
+    "tl_linear_decode_f32act": (_I, [_P, _P, _P, _I, _I, _I, _P, _I, _P]),
     "tl_codec_quant": (_I, [_P, _I, _I, _P, _P, _P]),
     "tl_codec_dequant_add": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "tl_get_status": (_I, [_P]),
@@ -211,6 +213,31 @@ def tl_linear_decode_fused(packed, qT, sw, x, N: int, K: int, y_dtype: int = TL_
     _check(lib().tl_linear_decode_fused(_ptr(packed), _ptr(qT), _ptr(sw), _ptr(x), _ptr(signs), M, N, K,
                                         _ptr(y), y_dtype, _ptr(acc_dbg), _ptr(xq_out), _ptr(sx_out),
                                         _stream(stream)), "tl_linear_decode_fused")
+    return y
+
+
+def tl_rotate_act(x: torch.Tensor, signs: torch.Tensor | None = None, xr: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """x bf16 [M,K] (device) -> xr fp32 [M,K], the rotation alone."""
+    _dev_tensor(x, torch.bfloat16, "x")
+    M, K = x.shape
+    if xr is None:
+        xr = torch.empty((M, K), dtype=torch.float32, device=x.device)
+    if signs is not None:
+        _dev_tensor(signs, torch.int8, "signs")
+    _check(lib().tl_rotate_act(_ptr(x), M, K, _ptr(signs), _ptr(xr), _stream(stream)), "tl_rotate_act")
+    return xr
+
+
+def tl_linear_decode_f32act(packed, s, xr, N: int, K: int, y_dtype: int = TL_F32,
+                            y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Float-activation decode (M <= 4): s fp16 [N,K/128], xr fp32 [M,K] -> y [M,N]."""
+    _dev_tensor(xr, torch.float32, "xr")
+    _dev_tensor(s, torch.float16, "s")
+    M = xr.shape[0]
+    y = _linear_out(M, N, y_dtype, xr.device, y)
+    _check(lib().tl_linear_decode_f32act(_ptr(packed), _ptr(s), _ptr(xr), M, N, K, _ptr(y), y_dtype,
+                                         _stream(stream)), "tl_linear_decode_f32act")
     return y
 
 

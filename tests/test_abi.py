@@ -103,3 +103,20 @@ def test_codec_argument_errors_without_gpu(lib):
     assert lib.tl_codec_dequant_add(ok, None, ok, 1, 4, 256, ok, None) == tl.TL_EINVAL
     assert lib.tl_codec_dequant_add(ok, ok, ok, 1, 4, 256, bad, None) == tl.TL_EINVAL
     assert lib.tl_codec_dequant_add(None, None, None, 1, 0, 256, None, None) == tl.TL_OK
+
+
+def test_float_decode_argument_errors_without_gpu(lib):
+    from quantized_linear_layers_block_gb300 import tl
+    P = ctypes.c_void_p
+    bad = P(16 + 8)
+    ok = P(4096)
+    assert lib.tl_linear_decode_f32act(ok, ok, ok, 5, 128, 1024, ok, tl.TL_F32, None) == tl.TL_EUNSUPPORTED
+    assert lib.tl_linear_decode_f32act(ok, ok, ok, 4, 128, 10240, ok, tl.TL_F32, None) == tl.TL_EUNSUPPORTED
+    assert lib.tl_linear_decode_f32act(ok, ok, ok, 1, 128, 1000, ok, tl.TL_F32, None) == tl.TL_EUNSUPPORTED
+    assert lib.tl_linear_decode_f32act(ok, None, ok, 1, 128, 1024, ok, tl.TL_F32, None) == tl.TL_EINVAL
+    assert lib.tl_linear_decode_f32act(ok, ok, bad, 1, 128, 1024, ok, tl.TL_F32, None) == tl.TL_EINVAL
+    assert lib.tl_linear_decode_f32act(ok, ok, ok, 1, 128, 1024, ok, tl.TL_I8, None) == tl.TL_EINVAL
+    assert lib.tl_linear_decode_f32act(None, None, None, 0, 128, 1024, None, tl.TL_F32, None) == tl.TL_OK
+    assert lib.tl_rotate_act(ok, 1, 1536, None, ok, None) == tl.TL_EUNSUPPORTED
+    assert lib.tl_rotate_act(ok, 1, 1024, bad, ok, None) == tl.TL_EINVAL
+    assert lib.tl_rotate_act(None, 0, 1024, None, None, None) == tl.TL_OK
