@@ -228,26 +228,17 @@ def main(argv=None):
 
     LAYERS = args.layers
     ws, rank, local = dist_info()
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
     import __graft_entry__
     __graft_entry__.build()
     from quantized_linear_layers_block_gb300 import synth, tl
+    from quantized_linear_layers_block_gb300.replicas import Replicas
 
-    def barrier():
-        if ws > 1:
-            torch.distributed.barrier()
-
-    def max_over_ranks(v: float) -> float:
-        if ws == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+    reps_ = Replicas(device=dev)      # replicas: no exchange on the data path
+    barrier = reps_.barrier
+    max_over_ranks = reps_.max
 
     # ---------------- inputs: 64 layer buffers per workload, resident in HBM
     P, D = PREFILL, DECODE
@@ -486,8 +477,7 @@ def main(argv=None):
                                           "kind": "oracle", "sample": dsample}
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if ws > 1:
-        torch.distributed.destroy_process_group()
+    reps_.close()
     return 0
 
 

@@ -258,6 +258,16 @@ int tl_codec_dequant_add(const uint16_t* own, const int8_t* q_peers, const float
                          int npeers, int R, int H, uint16_t* out, void* stream);
 
 /*
+ * Diagnostic: launches one kernel whose bounded wait can never be satisfied (an
+ * mbarrier phase nothing arrives at) with a limit of limit_us microseconds
+ * (1..100000, else TL_EINVAL). The wait gives up and records TL_ETIMEOUT in
+ * the device status word, which the next tl_get_status returns; the CUDA
+ * context stays usable. It checks the timeout path every kernel of the
+ * library takes when one of its waits runs out (those use a 2 s limit).
+ */
+int tl_selftest_wait_timeout(unsigned int limit_us, void* stream);
+
+/*
  * Synchronises `stream`, then returns and clears the current device's status
  * word: TL_OK, TL_ETIMEOUT or TL_EDATA (first error recorded), or TL_ECUDA if
  * the synchronisation itself failed.

@@ -53,6 +53,20 @@ int check_linear(const void* packed, const void* qT, const void* sw, const void*
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
+// A wait that nothing ends: phase 0 of a fresh mbarrier with no arrival. The
+// bounded wait gives up after limit_ns and records TL_ETIMEOUT, the path every
+// kernel of the library takes when one of its waits runs out.
+__global__ void wait_selftest_kernel(int* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    tl::mbar_init(tl::smem_u32(&bar), 1);
+    tl::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !tl::mbar_wait(tl::smem_u32(&bar), 0, nullptr, limit_ns))
+    tl::set_status(status, TL_ETIMEOUT);
+}
+
 }  // namespace
 
 extern "C" {
@@ -232,6 +246,15 @@ int tl_codec_dequant_add(const uint16_t* own, const int8_t* q_peers, const float
                                       as_stream(stream)) == cudaSuccess
              ? TL_OK
              : TL_ECUDA;
+}
+
+int tl_selftest_wait_timeout(unsigned int limit_us, void* stream) {
+  if (limit_us == 0 || limit_us > 100000) return TL_EINVAL;
+  int* status = nullptr;
+  const int r = status_ptr(&status);
+  if (r != TL_OK) return r;
+  wait_selftest_kernel<<<1, 32, 0, as_stream(stream)>>>(status, 1000ull * limit_us);
+  return cudaGetLastError() == cudaSuccess ? TL_OK : TL_ECUDA;
 }
 
 int tl_get_status(void* stream) {

@@ -42,6 +42,7 @@ SIGNATURES = {
     "tl_linear_decode_f32act": (_I, [_P, _P, _P, _I, _I, _I, _P, _I, _P]),
     "tl_codec_quant": (_I, [_P, _I, _I, _P, _P, _P]),
     "tl_codec_dequant_add": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
+    "tl_selftest_wait_timeout": (_I, [ctypes.c_uint, _P]),
     "tl_get_status": (_I, [_P]),
 }
 
@@ -269,6 +270,11 @@ def tl_codec_dequant_add(own: torch.Tensor, q_peers: torch.Tensor | None, scale_
     _check(lib().tl_codec_dequant_add(_ptr(own), _ptr(q_peers), _ptr(scale_peers), npeers, R, H, _ptr(out),
                                       _stream(stream)), "tl_codec_dequant_add")
     return out
+
+
+def tl_selftest_wait_timeout(limit_us: int = 2000, stream=None) -> None:
+    """Launch the library's wait that cannot complete (see include/tl.h); tl_get_status then reads TL_ETIMEOUT."""
+    _check(lib().tl_selftest_wait_timeout(int(limit_us), _stream(stream)), "tl_selftest_wait_timeout")
 
 
 def tl_get_status(stream=None) -> int:
