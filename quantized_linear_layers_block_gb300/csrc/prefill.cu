@@ -15,28 +15,33 @@
 //
 // Work: persistent CTAs (one per SM) over output tiles of 128 weight rows x
 // 128 tokens; the MMA computes D[n, m] = sum_k W[n, k] X[m, k] (y transposed,
-// weight rows on the tensor-memory lanes), 64 columns of K per stage.
+// weight rows on the tensor-memory lanes), 256 columns of K per pipeline
+// stage (16 MMAs of K = 16).
 // Roles of the 20 warps:
-//   warp 0       weight producer: packed 2-bit codes of the 128 rows and their q
-//                bytes per stage into a 16-deep ring; it starts before the kernel
-//                waits for the preceding one (programmatic dependent launch).
+//   warp 0       weight producer: packed 2-bit codes of the 128 rows and their
+//                two q bytes per row and stage into a 4-deep ring (TMA); it
+//                starts before the kernel waits for the preceding one
+//                (programmatic dependent launch).
 //   warp 2       activation producer: after that wait, the fp16 activation tile
-//                per stage (128-byte swizzle) into an 8-deep ring.
-//   warp 1       allocates tensor memory; one thread issues the MMAs.
-//   warps 4-11   expansion, two warps per 32-lane quarter of tensor memory taking
-//                alternate stages: lane = weight row; 64 codes and q become 32
-//                fp16 pairs in registers, stored into tensor memory as the MMA's A
-//                operand (tcgen05.st). A slot is refilled as soon as the MMA that
-//                read it completes (the MMA's commit releases it directly).
+//                of the stage (four 128-byte-swizzled boxes of 64 columns) into a
+//                3-deep ring.
+//   warp 1       allocates tensor memory; one thread issues the MMAs. It waits
+//                once per stage (on the A slot, whose expansion warps also saw
+//                the activations land), issues the stage's 16 MMAs and commits
+//                the A slot and the activation slot free: any other instruction
+//                in that thread costs tensor-pipe time, so it does nothing else.
+//   warps 4-11   expansion, two warps per 32-lane quarter of tensor memory: lane
+//                = weight row; warp `part` (0 or 1) turns the 128 codes of q
+//                group `part` of the stage into 64 fp16 pairs in registers and
+//                stores them into tensor memory as the MMA's A operand
+//                (tcgen05.st), then waits for the stage's activations and
+//                arrives on the A slot's full barrier.
 //   warps 12-19  drain + epilogue, two per quarter (64 tokens each): after each
-//                chunk add the fp32 accumulator (double buffered) into int32
-//                totals in registers; at the end of a tile write
+//                1024-column chunk add the fp32 accumulator (double buffered)
+//                into int32 totals in registers; at the end of a tile write
 //                y = (fl32(acc) sw[n]) sx[m].
-// Tensor memory (512 columns x 128 lanes): 8 A slots [0,256), fp32
-// accumulators [256,384) and [384,512).
-// The depth of each ring covers its recycling latency: an A slot goes round
-// MMA completion -> commit -> expansion -> MMA issue (two mbarrier hops plus
-// the expansion); a weight or activation slot adds the copy's latency.
+// Tensor memory (512 columns x 128 lanes): 2 A slots of 128 columns at [0,256),
+// fp32 accumulators at [256,384) and [384,512).
 // When the problem has fewer tiles than SMs, K is split across CTAs; partial
 // int32 sums meet in a caller workspace and the last CTA of a tile finishes it.
 #include "tl_internal.cuh"
