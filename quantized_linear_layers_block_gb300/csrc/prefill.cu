@@ -96,18 +96,34 @@ struct Smem {
 };
 static_assert(Smem::total + 1024 <= 232448, "shared memory budget");
 
+// Units of work: tiles [0, full) whole (all K chunks), then every remaining
+// tile split along K into `split` units of chunks. With at least as many tiles
+// as SMs only the last, partial round is split (so that round costs about
+// 1/split of a tile instead of a whole one); with fewer tiles than SMs every
+// tile is split. A split tile's partial int32 sums meet in workspace slot
+// tile - full.
 struct Work {
-  int units, split, mtiles, chunks;
+  int units, full, split, mtiles, chunks;
 };
 
 __device__ __forceinline__ void unit_coords(const Work& w, int u, int& nt, int& mt, int& c0,
-                                            int& c1) {
-  const int tile = u / w.split;
-  const int sp = u % w.split;
+                                            int& c1, int& slot) {
+  int tile;
+  if (u < w.full) {
+    tile = u;
+    c0 = 0;
+    c1 = w.chunks;
+    slot = -1;
+  } else {
+    const int v = u - w.full;
+    const int sp = v % w.split;
+    slot = v / w.split;
+    tile = w.full + slot;
+    c0 = sp * w.chunks / w.split;
+    c1 = (sp + 1) * w.chunks / w.split;
+  }
   mt = tile % w.mtiles;
   nt = tile / w.mtiles;
-  c0 = sp * w.chunks / w.split;
-  c1 = (sp + 1) * w.chunks / w.split;
 }
 
 __device__ __forceinline__ void store_out(void* y, int y_dtype, size_t idx, float v) {
@@ -227,8 +243,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
       uint32_t it = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < work.units; u += gridDim.x) {
-        int nt, mt, c0, c1;
-        unit_coords(work, u, nt, mt, c0, c1);
+        int nt, mt, c0, c1, slot;
+        unit_coords(work, u, nt, mt, c0, c1, slot);
         for (int c = c0; ok && c < c1; ++c) {
           for (int st = 0; st < STAGES_PER_CHUNK; ++st, ++it) {
             const int w = it % NW;
@@ -259,8 +275,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
       uint32_t it = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < work.units; u += gridDim.x) {
-        int nt, mt, c0, c1;
-        unit_coords(work, u, nt, mt, c0, c1);
+        int nt, mt, c0, c1, slot;
+        unit_coords(work, u, nt, mt, c0, c1, slot);
         for (int c = c0; ok && c < c1; ++c) {
           for (int st = 0; st < STAGES_PER_CHUNK; ++st, ++it) {
             const int b = it % NB;
@@ -293,8 +309,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
       // 16 KB apart, slots 64 KB apart, and each 16-column step is 32 bytes
       const uint64_t desc0 = smem_desc_sw128(sbase + Smem::b);
       for (int u = blockIdx.x; ok && u < work.units; u += gridDim.x) {
-        int nt, mt, c0, c1;
-        unit_coords(work, u, nt, mt, c0, c1);
+        int nt, mt, c0, c1, slot;
+        unit_coords(work, u, nt, mt, c0, c1, slot);
         for (int c = c0; ok && c < c1; ++c, ++cc) {
           const uint32_t buf = cc & 1u;
           const uint32_t dph = (cc >> 1) & 1u;
@@ -344,8 +360,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
     uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < work.units; u += gridDim.x) {
-      int nt, mt, c0, c1;
-      unit_coords(work, u, nt, mt, c0, c1);
+      int nt, mt, c0, c1, slot;
+      unit_coords(work, u, nt, mt, c0, c1, slot);
       for (int c = c0; ok && c < c1; ++c) {
         for (int st = 0; st < STAGES_PER_CHUNK; ++st, ++it) {
           const int w = it % NW;
@@ -409,8 +425,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
     uint32_t cc = 0, ku = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < work.units; u += gridDim.x) {
-      int nt, mt, c0, c1;
-      unit_coords(work, u, nt, mt, c0, c1);
+      int nt, mt, c0, c1, slot;
+      unit_coords(work, u, nt, mt, c0, c1, slot);
       int tot[64];
 #pragma unroll
       for (int j = 0; j < 64; ++j) tot[j] = 0;
@@ -439,17 +455,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
       const int n = nt * BM + row;
       const int mbase = mt * BN + half * 64;
       bool finish = ok;
-      if (work.split > 1) {
+      if (slot >= 0) {
         // Rendezvous of the drain warps through two mbarriers (bounded waits):
-        // every warp adds its partial sums, the leader counts the tile's
-        // finished splits, and the CTA that completes the tile writes it.
+        // every warp adds its partial sums into the tile's workspace slot
+        // ([token][row] within the tile), the leader counts the tile's finished
+        // splits, and the CTA that completes the tile writes it.
+        int32_t* wsl = ws_acc + static_cast<size_t>(slot) * (BM * BN) + (half * 64) * BM + row;
         const uint32_t rp = ku & 1u;
         ++ku;
         if (ok) {
 #pragma unroll
           for (int j = 0; j < 64; ++j) {
             const int m = mbase + j;
-            if (m < M) atomicAdd(ws_acc + static_cast<size_t>(m) * N + n, tot[j]);
+            if (m < M) atomicAdd(wsl + j * BM, tot[j]);
           }
           __threadfence();
         }
@@ -460,7 +478,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
           if (mbar_wait(rdv1, rp, abort_flag)) {
             if (!*abort_flag) {
               __threadfence();
-              last = atomicAdd(ws_cnt + u / work.split, 1) == work.split - 1;
+              last = atomicAdd(ws_cnt + slot, 1) == work.split - 1;
             }
           } else {
             fail();
@@ -479,7 +497,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
 #pragma unroll
           for (int j = 0; j < 64; ++j) {
             const int m = mbase + j;
-            if (m < M) tot[j] = __ldcg(ws_acc + static_cast<size_t>(m) * N + n);
+            if (m < M) tot[j] = __ldcg(wsl + j * BM);
           }
         }
       }
@@ -535,19 +553,38 @@ bool make_map_2d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, CUtens
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int choose_split(int tiles, int chunks, int num_sms) {
-  if (tiles >= num_sms) return 1;
-  int s = (num_sms + tiles - 1) / tiles;
-  return s < chunks ? s : chunks;
+// The unit schedule of a problem: see Work. Returns the workspace bytes the
+// split tiles need (0 when nothing is split).
+size_t plan_work(int M, int N, int K, int num_sms, Work* w) {
+  w->mtiles = (M + BN - 1) / BN;
+  w->chunks = K / kBlock;
+  const int tiles = w->mtiles * (N / BM);
+  if (tiles < num_sms) {
+    w->full = 0;
+    const int s = (num_sms + tiles - 1) / tiles;
+    w->split = s < w->chunks ? s : w->chunks;
+  } else {
+    const int rem = tiles % num_sms;
+    int s = rem > 0 ? num_sms / rem : 1;
+    if (s > w->chunks) s = w->chunks;
+    w->split = s;
+    w->full = s > 1 ? tiles - rem : tiles;
+  }
+  if (w->split <= 1) {
+    w->split = 1;
+    w->full = tiles;
+  }
+  const int nsplit = tiles - w->full;
+  w->units = w->full + nsplit * w->split;
+  if (nsplit == 0) return 0;
+  return static_cast<size_t>(nsplit) * (BM * BN) * 4 + static_cast<size_t>(nsplit) * 4;
 }
 
 }  // namespace
 
 size_t prefill_workspace_bytes(int M, int N, int K, int num_sms) {
-  const int mtiles = (M + BN - 1) / BN;
-  const int tiles = mtiles * (N / BM);
-  if (choose_split(tiles, K / kBlock, num_sms) <= 1) return 0;
-  return static_cast<size_t>(M) * N * 4 + static_cast<size_t>(tiles) * 4;
+  Work w;
+  return plan_work(M, N, K, num_sms, &w);
 }
 
 int launch_prefill(const PrefillArgs& a, int* status, cudaStream_t st, cudaError_t* cerr) {
@@ -574,24 +611,23 @@ int launch_prefill(const PrefillArgs& a, int* status, cudaStream_t st, cudaError
   }
 
   Work w;
-  w.mtiles = (a.M + BN - 1) / BN;
-  w.chunks = a.K / kBlock;
+  const size_t need = plan_work(a.M, a.N, a.K, num_sms, &w);
   const int tiles = w.mtiles * (a.N / BM);
-  w.split = choose_split(tiles, w.chunks, num_sms);
   int32_t* ws_acc = nullptr;
   int* ws_cnt = nullptr;
-  if (w.split > 1) {
-    const size_t need = static_cast<size_t>(a.M) * a.N * 4 + static_cast<size_t>(tiles) * 4;
+  if (need > 0) {
     if (a.workspace == nullptr || a.ws_bytes < need) {
-      w.split = 1;
+      w.split = 1;            // no room: every tile whole
+      w.full = tiles;
+      w.units = tiles;
     } else {
+      const int nsplit = tiles - w.full;
       ws_acc = static_cast<int32_t*>(a.workspace);
       ws_cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(a.workspace) +
-                                      static_cast<size_t>(a.M) * a.N * 4);
+                                      static_cast<size_t>(nsplit) * (BM * BN) * 4);
       if ((*cerr = cudaMemsetAsync(a.workspace, 0, need, st)) != cudaSuccess) return TL_ECUDA;
     }
   }
-  w.units = tiles * w.split;
   const int grid = w.units < num_sms ? w.units : num_sms;
   const size_t smem = Smem::total + 1024;
   if ((*cerr = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
