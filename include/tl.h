@@ -105,8 +105,11 @@ int tl_rotate_quant_act(const uint16_t* x, int M, int K, const int8_t* signs,
 
 /*
  * Workspace bytes that let tl_linear_prefill split the K dimension across
- * CTAs when an M x N problem has too few output tiles to fill the GPU.
- * With a smaller (or NULL) workspace the call still succeeds, unsplit.
+ * CTAs: the output tiles that do not fill a whole round of SMs (all of them
+ * when there are fewer tiles than SMs) are cut into equal ranges of
+ * 1024-column chunks, one per CTA, and a cut tile's partial int32 sums meet in
+ * a 64 KB slot of the workspace (plus 4 bytes per slot). With a smaller (or
+ * NULL) workspace the call still succeeds, unsplit.
  */
 int tl_prefill_workspace_size(int M, int N, int K, size_t* bytes);
 
@@ -179,12 +182,14 @@ int tl_linear_decode_fused(const uint8_t* packed, const int8_t* qT, const float*
  * where the scratch lives.)
  *
  * Arguments, layout, result and errors are those of tl_linear_prefill. When
- * the problem has few output tiles the K dimension is split and the partial
+ * the problem has fewer output tiles than SMs, K is split and the partial
  * int32 sums meet in a static device array of TL_NOALLOC_SCRATCH_BYTES owned
  * by the library; the call clears the part it uses before the kernel. If that
- * part would exceed the array (M * N * 4 bytes plus 4 bytes per output tile,
- * see tl_prefill_workspace_size) the call returns TL_ENOSPACE and launches
- * nothing. The call allocates nothing and calls no allocating routine.
+ * part would exceed the array (see tl_prefill_workspace_size) the call returns
+ * TL_ENOSPACE and launches nothing. With at least as many tiles as SMs only
+ * the last partial round is split; if that does not fit either, every tile
+ * runs whole (same result). The call allocates nothing and calls no
+ * allocating routine.
  *
  * - Every call shares the one array per device: calls that can overlap on the
  *   GPU (other streams, other host threads) race on it; serialise them.

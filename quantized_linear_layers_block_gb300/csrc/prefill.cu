@@ -96,34 +96,62 @@ struct Smem {
 };
 static_assert(Smem::total + 1024 <= 232448, "shared memory budget");
 
-// Units of work: tiles [0, full) whole (all K chunks), then every remaining
-// tile split along K into `split` units of chunks. With at least as many tiles
-// as SMs only the last, partial round is split (so that round costs about
-// 1/split of a tile instead of a whole one); with fewer tiles than SMs every
-// tile is split. A split tile's partial int32 sums meet in workspace slot
-// tile - full.
+// Work schedule. Tiles [0, full) are whole units, dealt round-robin to the
+// grid (full is a multiple of the grid, so every CTA gets the same number).
+// The remaining `tail` tiles form a chunk space of tail * chunks chunks that is
+// cut into `tgrid` contiguous, equal ranges, one per CTA 0 .. tgrid-1 (each at
+// least one chunk): a CTA's range covers pieces of one or more tiles. A tile
+// cut between CTAs meets in workspace slot (tile - full): every piece adds its
+// int32 partial sums there and the last of the tile's contributors writes it.
 struct Work {
-  int units, full, split, mtiles, chunks;
+  int mtiles, chunks, full, tail, tgrid;
 };
 
-__device__ __forceinline__ void unit_coords(const Work& w, int u, int& nt, int& mt, int& c0,
-                                            int& c1, int& slot) {
-  int tile;
-  if (u < w.full) {
-    tile = u;
-    c0 = 0;
-    c1 = w.chunks;
-    slot = -1;
-  } else {
-    const int v = u - w.full;
-    const int sp = v % w.split;
-    slot = v / w.split;
-    tile = w.full + slot;
-    c0 = sp * w.chunks / w.split;
-    c1 = (sp + 1) * w.chunks / w.split;
+struct Piece {
+  int nt, mt, c0, c1;   // tile (weight-row block, token block) and chunk range
+  int slot;             // workspace slot, or -1 for a whole tile
+  int contrib;          // CTAs that share the tile (1 for a whole tile)
+};
+
+__device__ __forceinline__ int num_pieces(const Work& w, int b) {
+  const int grid = static_cast<int>(gridDim.x);
+  int n = w.full > b ? (w.full - b - 1) / grid + 1 : 0;
+  if (b < w.tgrid) {
+    const int T = w.tail * w.chunks;
+    const int s = b * T / w.tgrid, e = (b + 1) * T / w.tgrid;
+    n += (e - 1) / w.chunks - s / w.chunks + 1;
   }
-  mt = tile % w.mtiles;
-  nt = tile / w.mtiles;
+  return n;
+}
+
+__device__ __forceinline__ Piece get_piece(const Work& w, int b, int k) {
+  const int grid = static_cast<int>(gridDim.x);
+  const int nfull = w.full > b ? (w.full - b - 1) / grid + 1 : 0;
+  Piece p;
+  int tile;
+  if (k < nfull) {
+    tile = b + k * grid;
+    p.c0 = 0;
+    p.c1 = w.chunks;
+    p.slot = -1;
+    p.contrib = 1;
+  } else {
+    const int T = w.tail * w.chunks;
+    const int s = b * T / w.tgrid, e = (b + 1) * T / w.tgrid;
+    const int tt = s / w.chunks + (k - nfull);          // tile within the tail
+    const int lo = tt * w.chunks, hi = lo + w.chunks;
+    p.c0 = (s > lo ? s : lo) - lo;
+    p.c1 = (e < hi ? e : hi) - lo;
+    // owner of chunk i: the CTA c with c T / tgrid <= i < (c + 1) T / tgrid
+    const int first = ((lo + 1) * w.tgrid - 1) / T;
+    const int last = (hi * w.tgrid - 1) / T;
+    p.contrib = last - first + 1;
+    p.slot = p.contrib > 1 ? tt : -1;
+    tile = w.full + tt;
+  }
+  p.mt = tile % w.mtiles;
+  p.nt = tile / w.mtiles;
+  return p;
 }
 
 __device__ __forceinline__ void store_out(void* y, int y_dtype, size_t idx, float v) {
@@ -242,9 +270,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
       tma_prefetch_desc(&map_q);
       uint32_t it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < work.units; u += gridDim.x) {
-        int nt, mt, c0, c1, slot;
-        unit_coords(work, u, nt, mt, c0, c1, slot);
+      const int npieces = num_pieces(work, blockIdx.x);
+      for (int k = 0; ok && k < npieces; ++k) {
+        const Piece pc = get_piece(work, blockIdx.x, k);
+        const int nt = pc.nt, c0 = pc.c0, c1 = pc.c1;
         for (int c = c0; ok && c < c1; ++c) {
           for (int st = 0; st < STAGES_PER_CHUNK; ++st, ++it) {
             const int w = it % NW;
@@ -274,9 +303,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
       pdl_wait_prior();
       uint32_t it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < work.units; u += gridDim.x) {
-        int nt, mt, c0, c1, slot;
-        unit_coords(work, u, nt, mt, c0, c1, slot);
+      const int npieces = num_pieces(work, blockIdx.x);
+      for (int k = 0; ok && k < npieces; ++k) {
+        const Piece pc = get_piece(work, blockIdx.x, k);
+        const int mt = pc.mt, c0 = pc.c0, c1 = pc.c1;
         for (int c = c0; ok && c < c1; ++c) {
           for (int st = 0; st < STAGES_PER_CHUNK; ++st, ++it) {
             const int b = it % NB;
@@ -308,9 +338,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
       // descriptor of activation slot 0, first box, first 16 columns: boxes are
       // 16 KB apart, slots 64 KB apart, and each 16-column step is 32 bytes
       const uint64_t desc0 = smem_desc_sw128(sbase + Smem::b);
-      for (int u = blockIdx.x; ok && u < work.units; u += gridDim.x) {
-        int nt, mt, c0, c1, slot;
-        unit_coords(work, u, nt, mt, c0, c1, slot);
+      const int npieces = num_pieces(work, blockIdx.x);
+      for (int k = 0; ok && k < npieces; ++k) {
+        const Piece pc = get_piece(work, blockIdx.x, k);
+        const int c0 = pc.c0, c1 = pc.c1;
         for (int c = c0; ok && c < c1; ++c, ++cc) {
           const uint32_t buf = cc & 1u;
           const uint32_t dph = (cc >> 1) & 1u;
@@ -359,9 +390,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     uint32_t it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < work.units; u += gridDim.x) {
-      int nt, mt, c0, c1, slot;
-      unit_coords(work, u, nt, mt, c0, c1, slot);
+    const int npieces = num_pieces(work, blockIdx.x);
+    for (int k = 0; ok && k < npieces; ++k) {
+      const Piece pc = get_piece(work, blockIdx.x, k);
+      const int c0 = pc.c0, c1 = pc.c1;
       for (int c = c0; ok && c < c1; ++c) {
         for (int st = 0; st < STAGES_PER_CHUNK; ++st, ++it) {
           const int w = it % NW;
@@ -380,6 +412,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
               reinterpret_cast<const uint4*>(smem + Smem::p + w * P_BYTES + row * (BK / 4) + part * 32);
           const uint4 pk0 = prow[0], pk1 = prow[1];
           const int qv = static_cast<int8_t>(smem[Smem::q + w * Q_BYTES + part * BM + row]);
+          // the slot is refilled by TMA (async proxy): order these ordinary
+          // loads before the release, or the copy can overtake them
+          fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(wempty(w));   // weight slot consumed
           const __half qh = __int2half_rn(qv);
@@ -424,9 +459,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     uint32_t cc = 0, ku = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < work.units; u += gridDim.x) {
-      int nt, mt, c0, c1, slot;
-      unit_coords(work, u, nt, mt, c0, c1, slot);
+    const int npieces = num_pieces(work, blockIdx.x);
+    for (int k = 0; ok && k < npieces; ++k) {
+      const Piece pc = get_piece(work, blockIdx.x, k);
+      const int nt = pc.nt, mt = pc.mt, c0 = pc.c0, c1 = pc.c1;
+      const int slot = pc.slot;
       int tot[64];
 #pragma unroll
       for (int j = 0; j < 64; ++j) tot[j] = 0;
@@ -478,7 +515,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
           if (mbar_wait(rdv1, rp, abort_flag)) {
             if (!*abort_flag) {
               __threadfence();
-              last = atomicAdd(ws_cnt + slot, 1) == work.split - 1;
+              last = atomicAdd(ws_cnt + slot, 1) == pc.contrib - 1;
             }
           } else {
             fail();
@@ -553,38 +590,43 @@ bool make_map_2d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, CUtens
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The unit schedule of a problem: see Work. Returns the workspace bytes the
-// split tiles need (0 when nothing is split).
-size_t plan_work(int M, int N, int K, int num_sms, Work* w) {
+// The schedule of a problem (see Work) on `grid` CTAs, and the workspace
+// bytes its split tiles need (0 when no tile is split).
+size_t plan_work(int M, int N, int K, int num_sms, Work* w, int* grid) {
   w->mtiles = (M + BN - 1) / BN;
   w->chunks = K / kBlock;
   const int tiles = w->mtiles * (N / BM);
-  if (tiles < num_sms) {
-    w->full = 0;
-    const int s = (num_sms + tiles - 1) / tiles;
-    w->split = s < w->chunks ? s : w->chunks;
+  if (tiles >= num_sms) {
+    *grid = num_sms;
+    w->full = tiles / num_sms * num_sms;
   } else {
-    const int rem = tiles % num_sms;
-    int s = rem > 0 ? num_sms / rem : 1;
-    if (s > w->chunks) s = w->chunks;
-    w->split = s;
-    w->full = s > 1 ? tiles - rem : tiles;
+    const int total = tiles * w->chunks;
+    *grid = total < num_sms ? total : num_sms;
+    w->full = 0;
   }
-  if (w->split <= 1) {
-    w->split = 1;
+  w->tail = tiles - w->full;
+  const int T = w->tail * w->chunks;
+  w->tgrid = T < *grid ? T : *grid;
+  if (w->tail == 0 || w->tgrid == w->tail) {
+    // nothing is cut: every tail tile is one CTA's whole range
     w->full = tiles;
+    w->tail = 0;
+    w->tgrid = 0;
+    return 0;
   }
-  const int nsplit = tiles - w->full;
-  w->units = w->full + nsplit * w->split;
-  if (nsplit == 0) return 0;
-  return static_cast<size_t>(nsplit) * (BM * BN) * 4 + static_cast<size_t>(nsplit) * 4;
+  return static_cast<size_t>(w->tail) * (BM * BN) * 4 + static_cast<size_t>(w->tail) * 4;
 }
 
 }  // namespace
 
 size_t prefill_workspace_bytes(int M, int N, int K, int num_sms) {
   Work w;
-  return plan_work(M, N, K, num_sms, &w);
+  int grid = 0;
+  return plan_work(M, N, K, num_sms, &w, &grid);
+}
+
+bool prefill_split_required(int M, int N, int num_sms) {
+  return ((M + BN - 1) / BN) * (N / BM) < num_sms;
 }
 
 int launch_prefill(const PrefillArgs& a, int* status, cudaStream_t st, cudaError_t* cerr) {
@@ -611,24 +653,24 @@ int launch_prefill(const PrefillArgs& a, int* status, cudaStream_t st, cudaError
   }
 
   Work w;
-  const size_t need = plan_work(a.M, a.N, a.K, num_sms, &w);
-  const int tiles = w.mtiles * (a.N / BM);
+  int grid = 0;
+  const size_t need = plan_work(a.M, a.N, a.K, num_sms, &w, &grid);
   int32_t* ws_acc = nullptr;
   int* ws_cnt = nullptr;
   if (need > 0) {
     if (a.workspace == nullptr || a.ws_bytes < need) {
-      w.split = 1;            // no room: every tile whole
-      w.full = tiles;
-      w.units = tiles;
+      // no room: every tile whole, dealt round-robin
+      w.full = w.mtiles * (a.N / BM);
+      w.tail = 0;
+      w.tgrid = 0;
+      if (grid > w.full) grid = w.full;
     } else {
-      const int nsplit = tiles - w.full;
       ws_acc = static_cast<int32_t*>(a.workspace);
       ws_cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(a.workspace) +
-                                      static_cast<size_t>(nsplit) * (BM * BN) * 4);
+                                      static_cast<size_t>(w.tail) * (BM * BN) * 4);
       if ((*cerr = cudaMemsetAsync(a.workspace, 0, need, st)) != cudaSuccess) return TL_ECUDA;
     }
   }
-  const int grid = w.units < num_sms ? w.units : num_sms;
   const size_t smem = Smem::total + 1024;
   if ((*cerr = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(smem))) != cudaSuccess)

@@ -160,7 +160,14 @@ int tl_linear_prefill_noalloc(const uint8_t* packed, const int8_t* qT, const flo
   if (r != TL_OK || M == 0 || N == 0) return r;
   size_t need = 0;
   if ((r = tl_prefill_workspace_size(M, N, K, &need)) != TL_OK) return r;
-  if (need > tl::kNoAllocScratchBytes) return TL_ENOSPACE;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return TL_ECUDA;
+  // with fewer tiles than SMs the split is the point: refuse what does not fit;
+  // otherwise only the last partial round would be split, and without room the
+  // kernel runs every tile whole
+  if (need > tl::kNoAllocScratchBytes && tl::prefill_split_required(M, N, sms)) return TL_ENOSPACE;
   int* status = nullptr;
   if ((r = status_ptr(&status)) != TL_OK) return r;
   void* scratch = nullptr;

@@ -74,6 +74,9 @@ cudaError_t launch_codec_quant(const uint16_t* x, int R, int H, int8_t* q, float
 cudaError_t launch_codec_dequant_add(const uint16_t* own, const int8_t* q, const float* scale,
                                      int npeers, int R, int H, uint16_t* out, cudaStream_t st);
 size_t prefill_workspace_bytes(int M, int N, int K, int num_sms);
+// True when the problem has fewer output tiles than SMs, so that splitting K
+// is what keeps the GPU busy (not only the last, partial round).
+bool prefill_split_required(int M, int N, int num_sms);
 // Returns TL_OK or a tl_status; *cerr receives the CUDA error when TL_ECUDA.
 int launch_prefill(const PrefillArgs& a, int* status, cudaStream_t st, cudaError_t* cerr);
 // Device address (this device) of the library-owned split-K scratch array of
@@ -119,6 +122,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Orders this thread's earlier generic-proxy accesses to shared memory before
+// later async-proxy accesses (a TMA copy) that another thread issues after
+// synchronising with it: required before releasing a shared-memory buffer
+// that was read with ordinary loads to a producer that refills it by TMA.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void fence_barrier_init() {

@@ -259,6 +259,24 @@ def test_prefill_split_k_matches_unsplit(tl):
     _compare(L, a1.cpu().numpy(), y1, 4)
 
 
+def test_prefill_repeatable_after_sync(tl):
+    """Whole tiles of 17 chunks on two CTAs, each call started on an idle GPU and
+    compared with the oracle: a shared-memory slot refilled by TMA while the
+    expansion warps' ordinary loads of it were still pending made rows of the
+    result wrong in some runs (fixed by a proxy fence before the slot's release)."""
+    L = synth.config_inputs("down_proj", M=64, N=256, K=17408)
+    packed, qT, sw = pack_dev(tl, L)
+    xq, sx = tl.tl_rotate_quant_act(x_dev(L), xq_dtype=tl.TL_F16)
+    ref = O.layer(L.x_bits, L.codes, L.s)["acc"]
+    for _ in range(8):
+        torch.cuda.synchronize()
+        a = torch.full((L.M, L.N), -7, dtype=torch.int32, device="cuda")
+        tl.tl_linear_prefill(packed, qT, sw, xq, sx, L.N, L.K, 4, acc_dbg=a, workspace=None)
+        torch.cuda.synchronize()
+        assert np.array_equal(a.cpu().numpy().astype(np.int64), ref)
+    check_status(tl)
+
+
 def test_exactness_adversarial(tl):
     """Chunk sums at the integer-exact fp32 limit, cancellation and +-1 terms.
 
