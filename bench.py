@@ -218,11 +218,16 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="layer buffers per step (64 = the model's depth; fewer only for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the benchmark line: the M sweep 1..4096 over both MLP shapes, "
+                         "one JSON line per point (prefill kernel, and decode kernel for M <= 32)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return reference_main(args)
+    if args.sweep:
+        return sweep_main(args)
 
     import torch
 
@@ -478,6 +483,65 @@ def main(argv=None):
     if rank == 0:
         print(json.dumps(line), flush=True)
     reps_.close()
+    return 0
+
+
+def sweep_main(args) -> int:
+    """The M sweep of the workloads: for each MLP shape 8 layer buffers (larger
+    than L2 together), and for each M the prefill kernel (and, for M <= 32, the
+    decode kernel) over the buffers, captured in a CUDA graph and timed with
+    CUDA events; rotate+quantise is outside the timed launches."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from quantized_linear_layers_block_gb300 import synth, tl
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    nl = 8
+    for name in ("sweep_up", "sweep_down"):
+        K, N = synth.CONFIGS[name]["K"], synth.CONFIGS[name]["N"]
+        layers = []
+        for li in range(nl):
+            codes, s, _ = synth.torch_config_layer(name, li, M=1, device=str(dev))
+            layers.append(tl.TernaryLinear(codes, s, device=dev))
+            del codes, s
+        for M in synth.SWEEP_M:
+            x = torch.randn((M, K), device=dev).to(torch.bfloat16)
+            xq16, sx = tl.tl_rotate_quant_act(x, xq_dtype=tl.TL_F16)
+            xq8, _ = tl.tl_rotate_quant_act(x, xq_dtype=tl.TL_I8)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ws = layers[0]._workspace(M)
+            runs = {"prefill": lambda l: tl.tl_linear_prefill(l.packed, l.qT, l.sw, xq16, sx, N, K, tl.TL_BF16,
+                                                              y=y, workspace=ws)}
+            if M <= 32:
+                runs["decode"] = lambda l: tl.tl_linear_decode(l.packed, l.qT, l.sw, xq8, sx, N, K, tl.TL_BF16, y=y)
+            line = {"shape": f"K={K} N={N}", "M": M}
+            for kind, fn in runs.items():
+                for l in layers:
+                    fn(l)
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()          # no host launch cost between the kernels
+                with torch.cuda.graph(g, capture_error_mode="relaxed"):
+                    for l in layers:
+                        fn(l)
+                g.replay()
+                torch.cuda.synchronize()
+                reps = max(3, min(40, int(4e5 // max(M, 64))))
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                us = 1e3 * e0.elapsed_time(e1) / (reps * nl)
+                line[f"{kind}_us"] = round(us, 2)
+                line[f"{kind}_tops"] = round(2.0 * M * N * K / (us * 1e-6) / 1e12, 1)
+                if M == 1:
+                    line[f"{kind}_weight_GB/s"] = round(weight_bytes(N, K) / (us * 1e-6) / 1e9, 1)
+            if tl.tl_get_status() != tl.TL_OK:
+                raise RuntimeError("device status during the sweep")
+            print(json.dumps(line), flush=True)
     return 0
 
 

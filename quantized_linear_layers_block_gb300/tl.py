@@ -286,12 +286,15 @@ class TernaryLinear:
 
     Built once from int8 codes [N,K] and fp16 group scales [N,K/128]; forward()
     takes bf16 activations [M,K] on the host or the device and returns y [M,N]
-    where it found x. M <= 32 runs rotate+quantise and the decode kernel, larger M
-    rotate+quantise and the tensor-core prefill kernel; both give the same
-    integer accumulator and the same y.
+    where it found x. Small M * K (decode) runs rotate+quantise and the CUDA-core
+    decode kernel, larger problems rotate+quantise and the tensor-core prefill
+    kernel; both give the same integer accumulator and the same y.
     """
 
-    DECODE_MAX_M = 32
+    # The CUDA-core decode kernel wins while M * K is small; above, the tensor-core
+    # prefill does (measured on GB300 over M = 1..32: decode is faster up to
+    # M = 8 at K = 5120 and up to M = 4 at K = 17408).
+    DECODE_MAX_MK = 72 * 1024
 
     def __init__(self, codes: torch.Tensor, s: torch.Tensor, device="cuda", y_dtype: int = TL_BF16):
         dev = torch.device(device)
@@ -316,7 +319,7 @@ class TernaryLinear:
         on_host = not x.is_cuda
         xd = x.to(self.device, non_blocking=True) if on_host else x
         M = xd.shape[0]
-        if M <= self.DECODE_MAX_M:
+        if M * self.K <= self.DECODE_MAX_MK:
             xq, sx = tl_rotate_quant_act(xd, xq_dtype=TL_I8, stream=stream)
             y = tl_linear_decode(self.packed, self.qT, self.sw, xq, sx, self.N, self.K,
                                  self.y_dtype, stream=stream)
