@@ -94,9 +94,21 @@ __device__ __forceinline__ void stage_q(const int8_t* __restrict__ qT, int N, in
 
 // ---------------------------------------------------------------- M = 1
 // PL chunks of 32 codes per lane and row (K = 1024 PL). Fully unrolled over
-// the warp's 4 rows and the PL chunks, so every ring slot is a register; RR
+// the warp's RPW rows and the PL chunks, so every ring slot is a register; RR
 // rows of weights are in flight per warp. The activations are staged once per
 // CTA as two half-chunk arrays (conflict-free 16-byte reads) with their sums.
+// Rows per warp: 4 while K <= 8192; 2 above, where one row fills the register
+// ring and 4-row CTAs would leave too few warps per SM for short N (down_proj,
+// K = 17408, N = 5120: 160 CTAs of 32 rows took 10.9 us, 320 of 16 take 8.2 us,
+// 640 of 8 need 1.4 waves at 78 registers and took 10.0 us).
+template <int PL>
+struct M1Traits {
+  static constexpr int RPW = PL <= 8 ? 4 : 2;                 // rows per warp
+  static constexpr int ROWS = kDecWarps * RPW;                // rows per CTA
+  static constexpr int RR = PL <= 4 ? 4 : (PL <= 8 ? 2 : 1);  // rows of weights in flight per warp
+  static constexpr int QSTRIDE = ROWS + 4;                    // padded q row: conflict-free reads
+};
+
 template <int PL>
 __global__ void __launch_bounds__(kDecWarps * 32)
 decode1_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ qT,
@@ -106,16 +118,19 @@ decode1_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ q
   constexpr int K = PL * kBlock;
   constexpr int G = K / kGroup;
   constexpr int NC = K / 32;                           // chunks per row
-  constexpr int RR = PL <= 4 ? 4 : (PL <= 8 ? 2 : 1);  // rows of weights in flight per warp
+  constexpr int RPW = M1Traits<PL>::RPW;
+  constexpr int ROWS = M1Traits<PL>::ROWS;
+  constexpr int RR = M1Traits<PL>::RR;
+  constexpr int QS = M1Traits<PL>::QSTRIDE;
   __shared__ __align__(16) uint4 xw0[NC];
   __shared__ __align__(16) uint4 xw1[NC];
   __shared__ int csum[NC];
-  __shared__ __align__(16) int8_t qs[G * kQStride];
+  __shared__ __align__(16) int8_t qs[G * QS];
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int n0 = blockIdx.x * kRowsPerCta;
+  const int n0 = blockIdx.x * ROWS;
   const uint2* pw = reinterpret_cast<const uint2*>(packed) + static_cast<size_t>(n0 + warp) * NC + lane;
   constexpr size_t kRowStep = static_cast<size_t>(kDecWarps) * NC;   // uint2 between a warp's rows
 
@@ -126,7 +141,12 @@ decode1_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ q
     for (int i = 0; i < PL; ++i) ring[j][i] = __ldg(pw + j * kRowStep + i * 32);
   }
   pdl_launch_dependents();
-  stage_q(qT, N, G, n0, qs);
+  // q of this CTA's rows for all groups (qT is group-major: ROWS contiguous bytes per group)
+  for (int i = tid; i < G * (ROWS / 4); i += blockDim.x) {
+    const int g = i / (ROWS / 4), r4 = i % (ROWS / 4);
+    *reinterpret_cast<uint32_t*>(qs + g * QS + 4 * r4) =
+        *reinterpret_cast<const uint32_t*>(qT + static_cast<size_t>(g) * N + n0 + 4 * r4);
+  }
   pdl_wait_prior();
   for (int c = tid; c < NC; c += blockDim.x) {
     const uint4* src = reinterpret_cast<const uint4*>(xq + 32 * c);
@@ -139,16 +159,16 @@ decode1_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ q
   const float sx0 = sx[0];
 
 #pragma unroll
-  for (int j = 0; j < kRowsPerWarp; ++j) {
+  for (int j = 0; j < RPW; ++j) {
     const int r = warp + kDecWarps * j;
     int acc = 0;
 #pragma unroll
     for (int i = 0; i < PL; ++i) {
       const int c = i * 32 + lane;
       const uint2 wv = ring[j % RR][i];
-      if (j + RR < kRowsPerWarp) ring[j % RR][i] = __ldg(pw + (j + RR) * kRowStep + i * 32);
+      if (j + RR < RPW) ring[j % RR][i] = __ldg(pw + (j + RR) * kRowStep + i * 32);
       const int t = dot_chunk(wv.x, wv.y, xw0[c], xw1[c], -csum[c]);
-      acc += static_cast<int>(qs[(8 * i + (lane >> 2)) * kQStride + r]) * t;
+      acc += static_cast<int>(qs[(8 * i + (lane >> 2)) * QS + r]) * t;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
@@ -473,7 +493,7 @@ template <int PL>
 cudaError_t launch_m1(const uint32_t* packed, const int8_t* qT, const float* sw, const int8_t* xq,
                       const float* sx, int N, void* y, int y_dtype, int32_t* acc_dbg,
                       cudaStream_t st) {
-  return launch_pdl(decode1_kernel<PL>, dim3(N / kRowsPerCta), dim3(kDecWarps * 32), 0, st,
+  return launch_pdl(decode1_kernel<PL>, dim3(N / M1Traits<PL>::ROWS), dim3(kDecWarps * 32), 0, st,
                     packed, qT, sw, xq, sx, N, y, y_dtype, acc_dbg);
 }
 
