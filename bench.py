@@ -16,8 +16,10 @@ Metric: "ternary linear int8 TOPS @M=512; decode GEMV weight-stream GB/s @M=1".
 
 Inputs are seeded synthetic draws with the workloads' shapes and distributions,
 generated on the device; they are resident in HBM before timing starts.
-`e2e` repeats both through TernaryLinear.forward with pinned host buffers
-(host->device copy of x and device->host copy of y inside the timed region).
+`e2e` repeats both through the public API with pinned host buffers: each step
+copies every layer's x in and its y back inside the timed region (prefill:
+TernaryLinear layers driven by tl.HostPipeline, copies overlapping the kernels;
+decode: the whole step as one tl.GraphStep CUDA graph).
 `--impl reference` times the CPU oracle instead (see oracle/).
 """
 
@@ -402,22 +404,40 @@ def main(argv=None):
     # ---------------- int8 128-group codec (compress, decompress-and-add), 1584 x 5120
     codec = codec_bench(dev, stream, max(4, args.warmup), max(8, K))
 
-    # ---------------- end to end through TernaryLinear.forward with pinned host buffers
+    # ---------------- end to end through the public API with pinned host buffers: every
+    # step copies each layer's input in and its output back, synchronised at the end of
+    # the step (prefill: tl.HostPipeline overlaps the copies with the neighbouring layers'
+    # kernels)
     e2e_steps = 0 if args.no_e2e else max(1, min(K, 8))
     e2e_dsteps = 0 if args.no_e2e else max(1, min(Kd, 64))
     xh_p = [x.cpu().pin_memory() for _, x, _ in pre_layers]
     xh_d = [x.cpu().pin_memory() for _, x, _ in dec_layers]
+    yh_p = [torch.empty((P["M"], P["N"]), dtype=torch.bfloat16).pin_memory() for _ in range(LAYERS)]
+    yh_d = [torch.empty((D["M"], D["N"]), dtype=torch.bfloat16).pin_memory() for _ in range(LAYERS)]
+    pipe = tl.HostPipeline(dev)
+    for li in range(LAYERS):                       # warm the pipeline's buffers
+        pipe.submit(pre_layers[li][0], xh_p[li], yh_p[li])
+        pipe.submit(dec_layers[li][0], xh_d[li], yh_d[li])
+    pipe.synchronize()
     torch.cuda.synchronize()
     barrier()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         for li in range(LAYERS):
-            pre_layers[li][0].forward(xh_p[li])
+            pipe.submit(pre_layers[li][0], xh_p[li], yh_p[li])
+        pipe.synchronize()
     e2e_pre_s = max(max_over_ranks(time.perf_counter() - t0), 1e-9)
+    # decode: the whole step (64 x: copy in, rotate+quantise, decode, copy out) is one
+    # CUDA graph (tl.GraphStep), one host launch per step
+    dstep = tl.GraphStep([dec_layers[li][0] for li in range(LAYERS)], [D["M"]] * LAYERS, dev)
+    for li in range(LAYERS):
+        dstep.inputs[li].copy_(xh_d[li])
+    for _ in range(3):
+        dstep.run()
+    barrier()
     t0 = time.perf_counter()
     for _ in range(e2e_dsteps):
-        for li in range(LAYERS):
-            dec_layers[li][0].forward(xh_d[li])
+        dstep.run()
     e2e_dec_s = max(max_over_ranks(time.perf_counter() - t0), 1e-9)
 
     # ---------------- figures

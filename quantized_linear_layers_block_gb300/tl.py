@@ -315,18 +315,19 @@ class TernaryLinear:
             self._ws = torch.empty((need,), dtype=torch.uint8, device=self.device)
         return self._ws
 
-    def forward(self, x: torch.Tensor, stream=None) -> torch.Tensor:
+    def forward(self, x: torch.Tensor, stream=None, out: torch.Tensor | None = None) -> torch.Tensor:
+        """y = layer(x). `out` (device, [M, N], the layer's y dtype) receives y when given."""
         on_host = not x.is_cuda
         xd = x.to(self.device, non_blocking=True) if on_host else x
         M = xd.shape[0]
         if M * self.K <= self.DECODE_MAX_MK:
             xq, sx = tl_rotate_quant_act(xd, xq_dtype=TL_I8, stream=stream)
             y = tl_linear_decode(self.packed, self.qT, self.sw, xq, sx, self.N, self.K,
-                                 self.y_dtype, stream=stream)
+                                 self.y_dtype, y=out, stream=stream)
         else:
             xq, sx = tl_rotate_quant_act(xd, xq_dtype=TL_F16, stream=stream)
             y = tl_linear_prefill(self.packed, self.qT, self.sw, xq, sx, self.N, self.K,
-                                  self.y_dtype, workspace=self._workspace(M), stream=stream)
+                                  self.y_dtype, y=out, workspace=self._workspace(M), stream=stream)
         if on_host:
             out = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
             out.copy_(y, non_blocking=True)
@@ -335,3 +336,117 @@ class TernaryLinear:
         return y
 
     __call__ = forward
+
+
+class HostPipeline:
+    """Runs TernaryLinear layers on host (pinned) inputs with the copies overlapped.
+
+    Three CUDA streams: host->device copies, the layer kernels, device->host
+    copies. submit() queues one layer call and returns at once; the copy of the
+    next input runs while the current layer computes, and the copy-back of a
+    result while the next layer computes. `depth` device input buffers rotate so
+    that a buffer is reused only after the kernels that read it have finished.
+    synchronize() waits for every submitted call; results are then in the pinned
+    host tensors given to submit(). The arithmetic is the layers' own (the
+    library's kernels); this class only orders copies and launches.
+    """
+
+    def __init__(self, device="cuda", depth: int = 3):
+        self.device = torch.device(device)
+        self.depth = depth
+        self.h2d = torch.cuda.Stream(self.device)
+        self.comp = torch.cuda.Stream(self.device)
+        self.d2h = torch.cuda.Stream(self.device)
+        self._xbuf = [None] * depth
+        self._free = [None] * depth     # event: the kernels reading buffer i have finished
+        self._n = 0
+
+    def submit(self, layer: "TernaryLinear", x_host: torch.Tensor, y_host: torch.Tensor) -> None:
+        if x_host.is_cuda or y_host.is_cuda:
+            raise ValueError("HostPipeline takes host tensors (pinned for overlap)")
+        i = self._n % self.depth
+        self._n += 1
+        buf = self._xbuf[i]
+        if buf is None or buf.shape != x_host.shape or buf.dtype != x_host.dtype:
+            buf = self._xbuf[i] = torch.empty(x_host.shape, dtype=x_host.dtype, device=self.device)
+        with torch.cuda.stream(self.h2d):
+            if self._free[i] is not None:
+                self.h2d.wait_event(self._free[i])
+            buf.copy_(x_host, non_blocking=True)
+            copied = torch.cuda.Event()
+            copied.record(self.h2d)
+        with torch.cuda.stream(self.comp):
+            self.comp.wait_event(copied)
+            y = layer.forward(buf, stream=self.comp)
+            done = torch.cuda.Event()
+            done.record(self.comp)
+            self._free[i] = done
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(done)
+            y.record_stream(self.d2h)
+            y_host.copy_(y, non_blocking=True)
+
+    def synchronize(self) -> None:
+        self.d2h.synchronize()
+        self.comp.synchronize()
+        self.h2d.synchronize()
+
+
+class GraphStep:
+    """One step of layer calls with host I/O, captured in a CUDA graph.
+
+    `layers` are TernaryLinear objects and `ms` their token counts. The step
+    owns one pinned host buffer for all inputs and one for all outputs, exposed
+    as per-layer views (`inputs[i]` bf16 [M_i, K_i], `outputs[i]` [M_i, N_i]).
+    run() replays: one host->device copy of every input, each layer's kernels
+    writing into a slice of one device output buffer, one device->host copy of
+    every output, then waits. A step costs one launch from the host however many
+    layers it holds (the serving pattern for decode, where a layer's kernels take
+    a few microseconds). Captured once on a side stream after one eager warm-up.
+    """
+
+    def __init__(self, layers, ms, device="cuda"):
+        self.device = torch.device(device)
+        self.layers = list(layers)
+        ms = list(ms)
+        dt = {TL_BF16: torch.bfloat16, TL_F32: torch.float32}
+        ydts = {l.y_dtype for l in self.layers}
+        if len(ydts) != 1:
+            raise ValueError("GraphStep layers must share one output dtype")
+        ydt = dt[ydts.pop()]
+        in_sizes = [m * l.K for l, m in zip(self.layers, ms)]
+        out_sizes = [m * l.N for l, m in zip(self.layers, ms)]
+        self._in_host = torch.empty(sum(in_sizes), dtype=torch.bfloat16).pin_memory()
+        self._out_host = torch.empty(sum(out_sizes), dtype=ydt).pin_memory()
+        self._in_dev = torch.empty(sum(in_sizes), dtype=torch.bfloat16, device=self.device)
+        self._out_dev = torch.empty(sum(out_sizes), dtype=ydt, device=self.device)
+
+        def views(buf, sizes, shapes):
+            out, o = [], 0
+            for n, shp in zip(sizes, shapes):
+                out.append(buf[o:o + n].view(shp))
+                o += n
+            return out
+        in_shapes = [(m, l.K) for l, m in zip(self.layers, ms)]
+        out_shapes = [(m, l.N) for l, m in zip(self.layers, ms)]
+        self.inputs = views(self._in_host, in_sizes, in_shapes)
+        self.outputs = views(self._out_host, out_sizes, out_shapes)
+        self._xd = views(self._in_dev, in_sizes, in_shapes)
+        self._yd = views(self._out_dev, out_sizes, out_shapes)
+        self._stream = torch.cuda.Stream(self.device)
+        with torch.cuda.stream(self._stream):
+            self._body()
+        self._stream.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self._stream, capture_error_mode="relaxed"):
+            self._body()
+
+    def _body(self):
+        self._in_dev.copy_(self._in_host, non_blocking=True)
+        for layer, xd, yd in zip(self.layers, self._xd, self._yd):
+            layer.forward(xd, out=yd)
+        self._out_host.copy_(self._out_dev, non_blocking=True)
+
+    def run(self) -> None:
+        self.graph.replay()
+        torch.cuda.current_stream(self.device).synchronize()

@@ -404,3 +404,45 @@ def test_argument_errors_launch_nothing(tl):
     assert lib.tl_rotate_quant_act(None, 0, 1024, None, None, 1, None, s) == tl.TL_OK
     assert torch.all(y == 0)
     check_status(tl)
+
+
+def test_host_pipeline_matches_forward(tl):
+    """tl.HostPipeline (copies overlapped with the kernels on three streams) gives the
+    same bytes as TernaryLinear.forward on device tensors, for decode and prefill sizes."""
+    outs = []
+    pipe = tl.HostPipeline("cuda", depth=2)
+    cases = []
+    for li, M in enumerate((1, 64, 3, 130, 16)):
+        L = synth.config_inputs("tiny", M=M)
+        lay = tl.TernaryLinear(torch.from_numpy(L.codes), torch.from_numpy(L.s))
+        xh = torch.from_numpy(L.x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+        yh = torch.empty((M, L.N), dtype=torch.bfloat16).pin_memory()
+        pipe.submit(lay, xh, yh)
+        cases.append((lay, xh, yh))
+    pipe.synchronize()
+    for lay, xh, yh in cases:
+        ref = lay.forward(xh.cuda())
+        torch.cuda.synchronize()
+        assert torch.equal(yh, ref.cpu())
+    check_status(tl)
+
+
+def test_graph_step_matches_forward(tl):
+    """tl.GraphStep (one copy in, the layers, one copy out, captured in a CUDA graph)
+    gives the same bytes as TernaryLinear.forward, on every replay, with new inputs."""
+    layers, ms, xs = [], [], []
+    for li, M in enumerate((1, 2, 16)):
+        L = synth.config_inputs("tiny", M=M)
+        layers.append(tl.TernaryLinear(torch.from_numpy(L.codes), torch.from_numpy(L.s)))
+        ms.append(M)
+        xs.append(torch.from_numpy(L.x_bits.view(np.int16)).view(torch.bfloat16))
+    step = tl.GraphStep(layers, ms)
+    for rep in range(3):
+        for x, xin in zip(xs, step.inputs):
+            xin.copy_(x if rep < 2 else -x)
+        step.run()
+        for lay, xin, yout in zip(layers, step.inputs, step.outputs):
+            ref = lay.forward(xin.cuda())
+            torch.cuda.synchronize()
+            assert torch.equal(yout, ref.cpu())
+    check_status(tl)
