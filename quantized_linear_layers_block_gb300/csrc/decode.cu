@@ -180,6 +180,134 @@ decode1_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ q
   }
 }
 
+// ---------------------------------------------------------------- 2 <= M <= 16, small M * K
+// The M = 1 kernel's layout for MT tokens (M rounded up to a power of two):
+// the masked code words of a chunk are formed once and taken into dp4a with
+// each token's staged activations (dynamic shared memory, MT * K * 9/8 bytes,
+// so MT * K is kept to 72 K). A warp's MT row sums are reduced together: at
+// each of log2(MT) exchange steps a lane keeps half of its tokens and adds the
+// partner's half of the same tokens (MT - 1 shuffles), then the remaining
+// 5 - log2(MT) butterfly steps finish the sum (instead of 5 MT shuffles).
+template <int PL, int MT>
+struct MTTraits {
+  static constexpr int RPW = PL <= 8 ? 4 : 2;                    // rows per warp
+  static constexpr int ROWS = kDecWarps * RPW;                   // rows per CTA
+  static constexpr int RR = (MT >= 8 || PL > 4) ? 1 : 2;         // rows of weights in flight
+  static constexpr int QSTRIDE = ROWS + 4;
+  static constexpr int LOG2MT = MT == 2 ? 1 : (MT == 4 ? 2 : (MT == 8 ? 3 : 4));
+  static constexpr size_t SMEM = static_cast<size_t>(MT) * (PL * kBlock / 32) * 36;
+};
+
+template <int PL, int MT>
+__global__ void __launch_bounds__(kDecWarps * 32)
+decodem_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ qT,
+               const float* __restrict__ sw, const int8_t* __restrict__ xq,
+               const float* __restrict__ sx, int M, int N, void* __restrict__ y, int y_dtype,
+               int32_t* __restrict__ acc_dbg) {
+  using T = MTTraits<PL, MT>;
+  constexpr int K = PL * kBlock;
+  constexpr int G = K / kGroup;
+  constexpr int NC = K / 32;
+  constexpr int RPW = T::RPW, ROWS = T::ROWS, RR = T::RR, QS = T::QSTRIDE;
+  extern __shared__ __align__(16) uint8_t dsm[];
+  uint4* xw0 = reinterpret_cast<uint4*>(dsm);            // [MT][NC]
+  uint4* xw1 = xw0 + MT * NC;                             // [MT][NC]
+  int* csum = reinterpret_cast<int*>(xw1 + MT * NC);      // [MT][NC]
+  __shared__ __align__(16) int8_t qs[G * QS];
+  __shared__ float sxs[MT];
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int n0 = blockIdx.x * ROWS;
+  const uint2* pw = reinterpret_cast<const uint2*>(packed) + static_cast<size_t>(n0 + warp) * NC + lane;
+  constexpr size_t kRowStep = static_cast<size_t>(kDecWarps) * NC;
+
+  uint2 ring[RR][PL];
+#pragma unroll
+  for (int j = 0; j < RR; ++j) {
+#pragma unroll
+    for (int i = 0; i < PL; ++i) ring[j][i] = __ldg(pw + j * kRowStep + i * 32);
+  }
+  pdl_launch_dependents();
+  for (int i = tid; i < G * (ROWS / 4); i += blockDim.x) {
+    const int g = i / (ROWS / 4), r4 = i % (ROWS / 4);
+    *reinterpret_cast<uint32_t*>(qs + g * QS + 4 * r4) =
+        *reinterpret_cast<const uint32_t*>(qT + static_cast<size_t>(g) * N + n0 + 4 * r4);
+  }
+  pdl_wait_prior();
+  for (int i = tid; i < MT * NC; i += blockDim.x) {
+    const int m = i / NC, c = i - m * NC;
+    uint4 u0 = make_uint4(0, 0, 0, 0), u1 = u0;
+    if (m < M) {
+      const uint4* src = reinterpret_cast<const uint4*>(xq + static_cast<size_t>(m) * K + 32 * c);
+      u0 = src[0];
+      u1 = src[1];
+    }
+    uint4 p0, p1;
+    csum[i] = permute_chunk(u0, u1, p0, p1);
+    xw0[i] = p0;
+    xw1[i] = p1;
+  }
+  if (tid < MT) sxs[tid] = tid < M ? sx[tid] : 0.f;
+  __syncthreads();
+
+#pragma unroll
+  for (int j = 0; j < RPW; ++j) {
+    const int r = warp + kDecWarps * j;
+    int acc[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc[m] = 0;
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+      const int c = i * 32 + lane;
+      const uint2 wv = ring[j % RR][i];
+      if (j + RR < RPW) ring[j % RR][i] = __ldg(pw + (j + RR) * kRowStep + i * 32);
+      const uint32_t e[8] = {wv.x & 0x03030303u, (wv.x >> 2) & 0x03030303u, (wv.x >> 4) & 0x03030303u,
+                             (wv.x >> 6) & 0x03030303u, wv.y & 0x03030303u, (wv.y >> 2) & 0x03030303u,
+                             (wv.y >> 4) & 0x03030303u, (wv.y >> 6) & 0x03030303u};
+      const int q = qs[(8 * i + (lane >> 2)) * QS + r];
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        const uint4 xa = xw0[m * NC + c], xb = xw1[m * NC + c];
+        int t = -csum[m * NC + c];
+        t = __dp4a(static_cast<int>(e[0]), static_cast<int>(xa.x), t);
+        t = __dp4a(static_cast<int>(e[1]), static_cast<int>(xa.y), t);
+        t = __dp4a(static_cast<int>(e[2]), static_cast<int>(xa.z), t);
+        t = __dp4a(static_cast<int>(e[3]), static_cast<int>(xa.w), t);
+        t = __dp4a(static_cast<int>(e[4]), static_cast<int>(xb.x), t);
+        t = __dp4a(static_cast<int>(e[5]), static_cast<int>(xb.y), t);
+        t = __dp4a(static_cast<int>(e[6]), static_cast<int>(xb.z), t);
+        t = __dp4a(static_cast<int>(e[7]), static_cast<int>(xb.w), t);
+        acc[m] += q * t;
+      }
+    }
+    // reduce-scatter over the tokens, then finish the sum of the lane's token
+    int tm = 0;
+#pragma unroll
+    for (int st = 0; st < T::LOG2MT; ++st) {
+      const int half = MT >> (st + 1);
+      const int o = 16 >> st;
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int k = 0; k < half; ++k) {
+        const int send = up ? acc[k] : acc[k + half];
+        const int keep = up ? acc[k + half] : acc[k];
+        acc[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+      if (up) tm += half;
+    }
+#pragma unroll
+    for (int o = 16 >> T::LOG2MT; o > 0; o >>= 1) acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
+    if ((lane & ((32 >> T::LOG2MT) - 1)) == 0 && tm < M) {
+      const int n = n0 + r;
+      const size_t idx = static_cast<size_t>(tm) * N + n;
+      if (acc_dbg != nullptr) acc_dbg[idx] = acc[0];
+      store_y(y, y_dtype, idx, __fmul_rn(__fmul_rn(__int2float_rn(acc[0]), sw[n]), sxs[tm]));
+    }
+  }
+}
+
 // ---------------------------------------------------------------- M = 1, fused
 // One launch for the whole layer at M = 1: the kernel takes the bf16 token,
 // and every CTA performs the input-side rotation and the per-token
@@ -497,6 +625,48 @@ cudaError_t launch_m1(const uint32_t* packed, const int8_t* qT, const float* sw,
                     packed, qT, sw, xq, sx, N, y, y_dtype, acc_dbg);
 }
 
+template <int PL, int MT>
+cudaError_t launch_mm(const uint32_t* packed, const int8_t* qT, const float* sw, const int8_t* xq,
+                      const float* sx, int M, int N, void* y, int y_dtype, int32_t* acc_dbg,
+                      cudaStream_t st) {
+  using T = MTTraits<PL, MT>;
+  if (T::SMEM > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(decodem_kernel<PL, MT>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(T::SMEM));
+    if (e != cudaSuccess) return e;
+  }
+  return launch_pdl(decodem_kernel<PL, MT>, dim3(N / T::ROWS), dim3(kDecWarps * 32), T::SMEM, st,
+                    packed, qT, sw, xq, sx, M, N, y, y_dtype, acc_dbg);
+}
+
+// The multi-token kernel for MT * K <= 72 K and the instantiated K; else -1.
+template <int MT>
+int try_mm(const uint32_t* packed, const int8_t* qT, const float* sw, const int8_t* xq,
+           const float* sx, int M, int N, int K, void* y, int y_dtype, int32_t* acc_dbg,
+           cudaStream_t st, cudaError_t* err) {
+  if (static_cast<long long>(MT) * K > 72 * 1024) return -1;
+  switch (K / kBlock) {
+    case 1: *err = launch_mm<1, MT>(packed, qT, sw, xq, sx, M, N, y, y_dtype, acc_dbg, st); return 0;
+    case 2: *err = launch_mm<2, MT>(packed, qT, sw, xq, sx, M, N, y, y_dtype, acc_dbg, st); return 0;
+    case 3: *err = launch_mm<3, MT>(packed, qT, sw, xq, sx, M, N, y, y_dtype, acc_dbg, st); return 0;
+    case 4: *err = launch_mm<4, MT>(packed, qT, sw, xq, sx, M, N, y, y_dtype, acc_dbg, st); return 0;
+    case 5:
+      if constexpr (MT <= 8) { *err = launch_mm<5, MT>(packed, qT, sw, xq, sx, M, N, y, y_dtype, acc_dbg, st); return 0; }
+      return -1;
+    case 8:
+      if constexpr (MT <= 8) { *err = launch_mm<8, MT>(packed, qT, sw, xq, sx, M, N, y, y_dtype, acc_dbg, st); return 0; }
+      return -1;
+    case 16:
+      if constexpr (MT <= 4) { *err = launch_mm<16, MT>(packed, qT, sw, xq, sx, M, N, y, y_dtype, acc_dbg, st); return 0; }
+      return -1;
+    case 17:
+      if constexpr (MT <= 4) { *err = launch_mm<17, MT>(packed, qT, sw, xq, sx, M, N, y, y_dtype, acc_dbg, st); return 0; }
+      return -1;
+    default: return -1;
+  }
+}
+
 template <int PL>
 cudaError_t launch_m1f(const uint32_t* packed, const int8_t* qT, const float* sw, const uint16_t* x,
                        const int8_t* signs, int N, void* y, int y_dtype, int32_t* acc_dbg,
@@ -530,6 +700,11 @@ cudaError_t launch_decode(const uint32_t* packed, const int8_t* qT, const float*
       default: break;
     }
   }
+  cudaError_t err = cudaSuccess;
+  if (M == 2 && try_mm<2>(packed, qT, sw, xq, sx, M, N, K, y, y_dtype, acc_dbg, st, &err) == 0) return err;
+  if (M >= 3 && M <= 4 && try_mm<4>(packed, qT, sw, xq, sx, M, N, K, y, y_dtype, acc_dbg, st, &err) == 0) return err;
+  if (M >= 5 && M <= 8 && try_mm<8>(packed, qT, sw, xq, sx, M, N, K, y, y_dtype, acc_dbg, st, &err) == 0) return err;
+  if (M >= 9 && M <= 16 && try_mm<16>(packed, qT, sw, xq, sx, M, N, K, y, y_dtype, acc_dbg, st, &err) == 0) return err;
   if (M <= 1) return launch_mt<1>(packed, qT, sw, xq, sx, M, N, K, y, y_dtype, acc_dbg, st);
   if (M <= 2) return launch_mt<2>(packed, qT, sw, xq, sx, M, N, K, y, y_dtype, acc_dbg, st);
   if (M <= 4) return launch_mt<4>(packed, qT, sw, xq, sx, M, N, K, y, y_dtype, acc_dbg, st);
