@@ -95,8 +95,11 @@ __device__ __forceinline__ void stage_q(const int8_t* __restrict__ qT, int N, in
 // ---------------------------------------------------------------- M = 1
 // PL chunks of 32 codes per lane and row (K = 1024 PL). Fully unrolled over
 // the warp's RPW rows and the PL chunks, so every ring slot is a register; RR
-// rows of weights are in flight per warp. The activations are staged once per
-// CTA as two half-chunk arrays (conflict-free 16-byte reads) with their sums.
+// rows of weights are in flight per warp and are worked in one group, so each
+// staged activation chunk is read once per RR rows (the 1-byte-per-code
+// shared-memory reads otherwise take as long as the arithmetic). The
+// activations are staged once per CTA as two half-chunk arrays (conflict-free
+// 16-byte reads) with their sums.
 // Rows per warp: 4 while K <= 8192; 2 above, where one row fills the register
 // ring and 4-row CTAs would leave too few warps per SM for short N (down_proj,
 // K = 17408, N = 5120: 160 CTAs of 32 rows took 10.9 us, 320 of 16 take 8.2 us,
@@ -158,24 +161,49 @@ decode1_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ q
   __syncthreads();
   const float sx0 = sx[0];
 
+  // rows in groups of RR (the rows whose weights are in the ring): each staged
+  // activation chunk is read from shared memory once per group, not once per row
 #pragma unroll
-  for (int j = 0; j < RPW; ++j) {
-    const int r = warp + kDecWarps * j;
-    int acc = 0;
+  for (int j0 = 0; j0 < RPW; j0 += RR) {
+    int acc[RR];
+#pragma unroll
+    for (int k = 0; k < RR; ++k) acc[k] = 0;
 #pragma unroll
     for (int i = 0; i < PL; ++i) {
       const int c = i * 32 + lane;
-      const uint2 wv = ring[j % RR][i];
-      if (j + RR < RPW) ring[j % RR][i] = __ldg(pw + (j + RR) * kRowStep + i * 32);
-      const int t = dot_chunk(wv.x, wv.y, xw0[c], xw1[c], -csum[c]);
-      acc += static_cast<int>(qs[(8 * i + (lane >> 2)) * QS + r]) * t;
+      const uint4 xa = xw0[c], xb = xw1[c];
+      const int cs = -csum[c];
+      const int8_t* qrow = qs + (8 * i + (lane >> 2)) * QS + warp;
+#pragma unroll
+      for (int k = 0; k < RR; ++k) {
+        const uint2 wv = ring[k][i];
+        if (j0 + RR < RPW) ring[k][i] = __ldg(pw + (j0 + RR + k) * kRowStep + i * 32);
+        const int t = dot_chunk(wv.x, wv.y, xa, xb, cs);
+        acc[k] += static_cast<int>(qrow[kDecWarps * (j0 + k)]) * t;
+      }
+    }
+    // the group's RR sums together: exchange halves, then the remaining butterfly steps
+    int tk = 0;
+    constexpr int LOG2RR = RR == 1 ? 0 : (RR == 2 ? 1 : 2);
+#pragma unroll
+    for (int st = 0; st < LOG2RR; ++st) {
+      const int half = RR >> (st + 1);
+      const int o = 16 >> st;
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int k = 0; k < half; ++k) {
+        const int send = up ? acc[k] : acc[k + half];
+        const int keep = up ? acc[k + half] : acc[k];
+        acc[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+      if (up) tk += half;
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) {
-      const int n = n0 + r;
-      if (acc_dbg != nullptr) acc_dbg[n] = acc;
-      store_y(y, y_dtype, n, __fmul_rn(__fmul_rn(__int2float_rn(acc), sw[n]), sx0));
+    for (int o = 16 >> LOG2RR; o > 0; o >>= 1) acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
+    if ((lane & ((32 >> LOG2RR) - 1)) == 0) {
+      const int n = n0 + warp + kDecWarps * (j0 + tk);
+      if (acc_dbg != nullptr) acc_dbg[n] = acc[0];
+      store_y(y, y_dtype, n, __fmul_rn(__fmul_rn(__int2float_rn(acc[0]), sw[n]), sx0));
     }
   }
 }
