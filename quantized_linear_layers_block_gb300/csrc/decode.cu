@@ -94,12 +94,12 @@ __device__ __forceinline__ void stage_q(const int8_t* __restrict__ qT, int N, in
 
 // ---------------------------------------------------------------- M = 1
 // PL chunks of 32 codes per lane and row (K = 1024 PL). Fully unrolled over
-// the warp's RPW rows and the PL chunks, so every ring slot is a register; RR
-// rows of weights are in flight per warp and are worked in one group, so each
-// staged activation chunk is read once per RR rows (the 1-byte-per-code
-// shared-memory reads otherwise take as long as the arithmetic). The
-// activations are staged once per CTA as two half-chunk arrays (conflict-free
-// 16-byte reads) with their sums.
+// the warp's RPW rows and the PL chunks, so every ring slot is a register. The
+// weight ring is chunk-major: RC chunk steps of all RPW rows in flight, so
+// each staged activation chunk is read from shared memory once for all the
+// warp's rows (reading it per row, 1 byte per code at 4 wavefronts per warp
+// load, took as long as the arithmetic). The activations are staged once per
+// CTA as two half-chunk arrays (conflict-free 16-byte reads) with their sums.
 // Rows per warp: 4 while K <= 8192; 2 above, where one row fills the register
 // ring and 4-row CTAs would leave too few warps per SM for short N (down_proj,
 // K = 17408, N = 5120: 160 CTAs of 32 rows took 10.9 us, 320 of 16 take 8.2 us,
@@ -108,7 +108,7 @@ template <int PL>
 struct M1Traits {
   static constexpr int RPW = PL <= 8 ? 4 : 2;                 // rows per warp
   static constexpr int ROWS = kDecWarps * RPW;                // rows per CTA
-  static constexpr int RR = PL <= 4 ? 4 : (PL <= 8 ? 2 : 1);  // rows of weights in flight per warp
+  static constexpr int RC = PL <= 4 ? PL : (PL <= 8 ? 3 : 8);  // chunk steps (of all RPW rows) in flight
   static constexpr int QSTRIDE = ROWS + 4;                    // padded q row: conflict-free reads
 };
 
@@ -123,7 +123,7 @@ decode1_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ q
   constexpr int NC = K / 32;                           // chunks per row
   constexpr int RPW = M1Traits<PL>::RPW;
   constexpr int ROWS = M1Traits<PL>::ROWS;
-  constexpr int RR = M1Traits<PL>::RR;
+  constexpr int RC = M1Traits<PL>::RC;
   constexpr int QS = M1Traits<PL>::QSTRIDE;
   __shared__ __align__(16) uint4 xw0[NC];
   __shared__ __align__(16) uint4 xw1[NC];
@@ -137,11 +137,12 @@ decode1_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ q
   const uint2* pw = reinterpret_cast<const uint2*>(packed) + static_cast<size_t>(n0 + warp) * NC + lane;
   constexpr size_t kRowStep = static_cast<size_t>(kDecWarps) * NC;   // uint2 between a warp's rows
 
-  uint2 ring[RR][PL];
+  // chunk-major ring: RC chunk steps, each holding the chunk of all RPW rows
+  uint2 ring[RC][RPW];
 #pragma unroll
-  for (int j = 0; j < RR; ++j) {
+  for (int i = 0; i < RC; ++i) {
 #pragma unroll
-    for (int i = 0; i < PL; ++i) ring[j][i] = __ldg(pw + j * kRowStep + i * 32);
+    for (int j = 0; j < RPW; ++j) ring[i][j] = __ldg(pw + j * kRowStep + i * 32);
   }
   pdl_launch_dependents();
   // q of this CTA's rows for all groups (qT is group-major: ROWS contiguous bytes per group)
@@ -161,50 +162,45 @@ decode1_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ q
   __syncthreads();
   const float sx0 = sx[0];
 
-  // rows in groups of RR (the rows whose weights are in the ring): each staged
-  // activation chunk is read from shared memory once per group, not once per row
+  int acc[RPW];
 #pragma unroll
-  for (int j0 = 0; j0 < RPW; j0 += RR) {
-    int acc[RR];
+  for (int k = 0; k < RPW; ++k) acc[k] = 0;
 #pragma unroll
-    for (int k = 0; k < RR; ++k) acc[k] = 0;
+  for (int i = 0; i < PL; ++i) {
+    const int c = i * 32 + lane;
+    const uint4 xa = xw0[c], xb = xw1[c];            // read once for all the warp's rows
+    const int cs = -csum[c];
+    const int8_t* qrow = qs + (8 * i + (lane >> 2)) * QS + warp;
 #pragma unroll
-    for (int i = 0; i < PL; ++i) {
-      const int c = i * 32 + lane;
-      const uint4 xa = xw0[c], xb = xw1[c];
-      const int cs = -csum[c];
-      const int8_t* qrow = qs + (8 * i + (lane >> 2)) * QS + warp;
-#pragma unroll
-      for (int k = 0; k < RR; ++k) {
-        const uint2 wv = ring[k][i];
-        if (j0 + RR < RPW) ring[k][i] = __ldg(pw + (j0 + RR + k) * kRowStep + i * 32);
-        const int t = dot_chunk(wv.x, wv.y, xa, xb, cs);
-        acc[k] += static_cast<int>(qrow[kDecWarps * (j0 + k)]) * t;
-      }
+    for (int k = 0; k < RPW; ++k) {
+      const uint2 wv = ring[i % RC][k];
+      if (i + RC < PL) ring[i % RC][k] = __ldg(pw + k * kRowStep + (i + RC) * 32);
+      const int t = dot_chunk(wv.x, wv.y, xa, xb, cs);
+      acc[k] += static_cast<int>(qrow[kDecWarps * k]) * t;
     }
-    // the group's RR sums together: exchange halves, then the remaining butterfly steps
-    int tk = 0;
-    constexpr int LOG2RR = RR == 1 ? 0 : (RR == 2 ? 1 : 2);
+  }
+  // the RPW sums together: exchange halves, then the remaining butterfly steps
+  int tk = 0;
+  constexpr int LOG2R = RPW == 1 ? 0 : (RPW == 2 ? 1 : 2);
 #pragma unroll
-    for (int st = 0; st < LOG2RR; ++st) {
-      const int half = RR >> (st + 1);
-      const int o = 16 >> st;
-      const bool up = (lane & o) != 0;
+  for (int st = 0; st < LOG2R; ++st) {
+    const int half = RPW >> (st + 1);
+    const int o = 16 >> st;
+    const bool up = (lane & o) != 0;
 #pragma unroll
-      for (int k = 0; k < half; ++k) {
-        const int send = up ? acc[k] : acc[k + half];
-        const int keep = up ? acc[k + half] : acc[k];
-        acc[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-      }
-      if (up) tk += half;
+    for (int k = 0; k < half; ++k) {
+      const int send = up ? acc[k] : acc[k + half];
+      const int keep = up ? acc[k + half] : acc[k];
+      acc[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
     }
+    if (up) tk += half;
+  }
 #pragma unroll
-    for (int o = 16 >> LOG2RR; o > 0; o >>= 1) acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
-    if ((lane & ((32 >> LOG2RR) - 1)) == 0) {
-      const int n = n0 + warp + kDecWarps * (j0 + tk);
-      if (acc_dbg != nullptr) acc_dbg[n] = acc[0];
-      store_y(y, y_dtype, n, __fmul_rn(__fmul_rn(__int2float_rn(acc[0]), sw[n]), sx0));
-    }
+  for (int o = 16 >> LOG2R; o > 0; o >>= 1) acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
+  if ((lane & ((32 >> LOG2R) - 1)) == 0) {
+    const int n = n0 + warp + kDecWarps * tk;
+    if (acc_dbg != nullptr) acc_dbg[n] = acc[0];
+    store_y(y, y_dtype, n, __fmul_rn(__fmul_rn(__int2float_rn(acc[0]), sw[n]), sx0));
   }
 }
 
