@@ -82,6 +82,22 @@ __device__ __forceinline__ int dot_chunk(uint32_t wa, uint32_t wb, uint4 xa, uin
   return t;
 }
 
+// The same sum with two masks per word: fields 0 and 2 (scale 1) and fields 1
+// and 3 (scale 4, exact: P + Q/4 with Q a multiple of 4).
+__device__ __forceinline__ int dot_chunk2(uint32_t wa, uint32_t wb, uint4 xa, uint4 xb, int t) {
+  const uint32_t wa4 = wa >> 4, wb4 = wb >> 4;
+  int p = t, q = 0;
+  p = __dp4a(static_cast<int>(wa & 0x03030303u), static_cast<int>(xa.x), p);
+  q = __dp4a(static_cast<int>(wa & 0x0C0C0C0Cu), static_cast<int>(xa.y), q);
+  p = __dp4a(static_cast<int>(wa4 & 0x03030303u), static_cast<int>(xa.z), p);
+  q = __dp4a(static_cast<int>(wa4 & 0x0C0C0C0Cu), static_cast<int>(xa.w), q);
+  p = __dp4a(static_cast<int>(wb & 0x03030303u), static_cast<int>(xb.x), p);
+  q = __dp4a(static_cast<int>(wb & 0x0C0C0C0Cu), static_cast<int>(xb.y), q);
+  p = __dp4a(static_cast<int>(wb4 & 0x03030303u), static_cast<int>(xb.z), p);
+  q = __dp4a(static_cast<int>(wb4 & 0x0C0C0C0Cu), static_cast<int>(xb.w), q);
+  return p + (q >> 2);
+}
+
 // q of this CTA's rows for all groups (qT is group-major: 32 contiguous bytes per group).
 __device__ __forceinline__ void stage_q(const int8_t* __restrict__ qT, int N, int G, int n0,
                                         int8_t* qs) {
@@ -175,7 +191,7 @@ decode1_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ q
     for (int k = 0; k < RPW; ++k) {
       const uint2 wv = ring[i % RC][k];
       if (i + RC < PL) ring[i % RC][k] = __ldg(pw + k * kRowStep + (i + RC) * 32);
-      const int t = dot_chunk(wv.x, wv.y, xa, xb, cs);
+      const int t = dot_chunk2(wv.x, wv.y, xa, xb, cs);
       acc[k] += static_cast<int>(qrow[kDecWarps * k]) * t;
     }
   }
@@ -344,19 +360,6 @@ decodem_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ q
 // sum = P + Q/4, exact since Q is a multiple of 4), and a warp reduces its four
 // row sums together (two exchange steps that halve the rows, then three
 // butterfly steps).
-__device__ __forceinline__ int dot_chunk2(uint32_t wa, uint32_t wb, uint4 xa, uint4 xb, int t) {
-  const uint32_t wa4 = wa >> 4, wb4 = wb >> 4;
-  int p = t, q = 0;
-  p = __dp4a(static_cast<int>(wa & 0x03030303u), static_cast<int>(xa.x), p);
-  q = __dp4a(static_cast<int>(wa & 0x0C0C0C0Cu), static_cast<int>(xa.y), q);
-  p = __dp4a(static_cast<int>(wa4 & 0x03030303u), static_cast<int>(xa.z), p);
-  q = __dp4a(static_cast<int>(wa4 & 0x0C0C0C0Cu), static_cast<int>(xa.w), q);
-  p = __dp4a(static_cast<int>(wb & 0x03030303u), static_cast<int>(xb.x), p);
-  q = __dp4a(static_cast<int>(wb & 0x0C0C0C0Cu), static_cast<int>(xb.y), q);
-  p = __dp4a(static_cast<int>(wb4 & 0x03030303u), static_cast<int>(xb.z), p);
-  q = __dp4a(static_cast<int>(wb4 & 0x0C0C0C0Cu), static_cast<int>(xb.w), q);
-  return p + (q >> 2);
-}
 
 constexpr int kFusedWarps = 32;
 constexpr int kFusedMaxQuads = kFusedWarps;
