@@ -222,9 +222,10 @@ decode1_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ q
 
 // ---------------------------------------------------------------- 2 <= M <= 16, small M * K
 // The M = 1 kernel's layout for MT tokens (M rounded up to a power of two):
-// the masked code words of a chunk are formed once and taken into dp4a with
-// each token's staged activations (dynamic shared memory, MT * K * 9/8 bytes,
-// so MT * K is kept to 72 K). A warp's MT row sums are reduced together: at
+// the masked code words of a chunk are formed once per row and taken into dp4a
+// with each token's staged activations (dynamic shared memory, MT * K * 9/8
+// bytes, so MT * K is kept to 72 K); GR rows share each activation read (the
+// reads cost MT bytes per code and bound the kernel when every row repeats them). A warp's MT row sums are reduced together: at
 // each of log2(MT) exchange steps a lane keeps half of its tokens and adds the
 // partner's half of the same tokens (MT - 1 shuffles), then the remaining
 // 5 - log2(MT) butterfly steps finish the sum (instead of 5 MT shuffles).
@@ -232,7 +233,9 @@ template <int PL, int MT>
 struct MTTraits {
   static constexpr int RPW = PL <= 8 ? 4 : 2;                    // rows per warp
   static constexpr int ROWS = kDecWarps * RPW;                   // rows per CTA
-  static constexpr int RR = (MT >= 8 || PL > 4) ? 1 : 2;         // rows of weights in flight
+  static constexpr int GR = MT >= 16 ? 1 : 2;                    // rows sharing one activation read
+  static constexpr int NG = RPW / GR;                            // row groups per warp
+  static constexpr int RC = PL * NG < 3 ? PL * NG : 3;           // (group, chunk) steps in flight
   static constexpr int QSTRIDE = ROWS + 4;
   static constexpr int LOG2MT = MT == 2 ? 1 : (MT == 4 ? 2 : (MT == 8 ? 3 : 4));
   static constexpr size_t SMEM = static_cast<size_t>(MT) * (PL * kBlock / 32) * 36;
@@ -248,7 +251,7 @@ decodem_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ q
   constexpr int K = PL * kBlock;
   constexpr int G = K / kGroup;
   constexpr int NC = K / 32;
-  constexpr int RPW = T::RPW, ROWS = T::ROWS, RR = T::RR, QS = T::QSTRIDE;
+  constexpr int ROWS = T::ROWS, GR = T::GR, NG = T::NG, RC = T::RC, QS = T::QSTRIDE;
   extern __shared__ __align__(16) uint8_t dsm[];
   uint4* xw0 = reinterpret_cast<uint4*>(dsm);            // [MT][NC]
   uint4* xw1 = xw0 + MT * NC;                             // [MT][NC]
@@ -263,11 +266,13 @@ decodem_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ q
   const uint2* pw = reinterpret_cast<const uint2*>(packed) + static_cast<size_t>(n0 + warp) * NC + lane;
   constexpr size_t kRowStep = static_cast<size_t>(kDecWarps) * NC;
 
-  uint2 ring[RR][PL];
+  // ring over the flattened (row group, chunk) steps t = g PL + i: GR rows' chunk i
+  uint2 ring[RC][GR];
 #pragma unroll
-  for (int j = 0; j < RR; ++j) {
+  for (int t = 0; t < RC; ++t) {
 #pragma unroll
-    for (int i = 0; i < PL; ++i) ring[j][i] = __ldg(pw + j * kRowStep + i * 32);
+    for (int k = 0; k < GR; ++k)
+      ring[t][k] = __ldg(pw + ((t / PL) * GR + k) * kRowStep + (t % PL) * 32);
   }
   pdl_launch_dependents();
   for (int i = tid; i < G * (ROWS / 4); i += blockDim.x) {
@@ -293,57 +298,77 @@ decodem_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ q
   __syncthreads();
 
 #pragma unroll
-  for (int j = 0; j < RPW; ++j) {
-    const int r = warp + kDecWarps * j;
-    int acc[MT];
+  for (int g = 0; g < NG; ++g) {
+    int acc[GR][MT];
 #pragma unroll
-    for (int m = 0; m < MT; ++m) acc[m] = 0;
+    for (int k = 0; k < GR; ++k)
+#pragma unroll
+      for (int m = 0; m < MT; ++m) acc[k][m] = 0;
 #pragma unroll
     for (int i = 0; i < PL; ++i) {
+      const int t = g * PL + i;
       const int c = i * 32 + lane;
-      const uint2 wv = ring[j % RR][i];
-      if (j + RR < RPW) ring[j % RR][i] = __ldg(pw + (j + RR) * kRowStep + i * 32);
-      const uint32_t e[8] = {wv.x & 0x03030303u, (wv.x >> 2) & 0x03030303u, (wv.x >> 4) & 0x03030303u,
-                             (wv.x >> 6) & 0x03030303u, wv.y & 0x03030303u, (wv.y >> 2) & 0x03030303u,
-                             (wv.y >> 4) & 0x03030303u, (wv.y >> 6) & 0x03030303u};
-      const int q = qs[(8 * i + (lane >> 2)) * QS + r];
+      uint32_t e[GR][8];
+      int q[GR];
+#pragma unroll
+      for (int k = 0; k < GR; ++k) {
+        const uint2 wv = ring[t % RC][k];
+        if (t + RC < NG * PL)
+          ring[t % RC][k] = __ldg(pw + (((t + RC) / PL) * GR + k) * kRowStep + ((t + RC) % PL) * 32);
+        e[k][0] = wv.x & 0x03030303u;
+        e[k][1] = (wv.x >> 2) & 0x03030303u;
+        e[k][2] = (wv.x >> 4) & 0x03030303u;
+        e[k][3] = (wv.x >> 6) & 0x03030303u;
+        e[k][4] = wv.y & 0x03030303u;
+        e[k][5] = (wv.y >> 2) & 0x03030303u;
+        e[k][6] = (wv.y >> 4) & 0x03030303u;
+        e[k][7] = (wv.y >> 6) & 0x03030303u;
+        q[k] = qs[(8 * i + (lane >> 2)) * QS + warp + kDecWarps * (g * GR + k)];
+      }
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
-        const uint4 xa = xw0[m * NC + c], xb = xw1[m * NC + c];
-        int t = -csum[m * NC + c];
-        t = __dp4a(static_cast<int>(e[0]), static_cast<int>(xa.x), t);
-        t = __dp4a(static_cast<int>(e[1]), static_cast<int>(xa.y), t);
-        t = __dp4a(static_cast<int>(e[2]), static_cast<int>(xa.z), t);
-        t = __dp4a(static_cast<int>(e[3]), static_cast<int>(xa.w), t);
-        t = __dp4a(static_cast<int>(e[4]), static_cast<int>(xb.x), t);
-        t = __dp4a(static_cast<int>(e[5]), static_cast<int>(xb.y), t);
-        t = __dp4a(static_cast<int>(e[6]), static_cast<int>(xb.z), t);
-        t = __dp4a(static_cast<int>(e[7]), static_cast<int>(xb.w), t);
-        acc[m] += q * t;
+        const uint4 xa = xw0[m * NC + c], xb = xw1[m * NC + c];   // one read for the GR rows
+        const int cs = -csum[m * NC + c];
+#pragma unroll
+        for (int k = 0; k < GR; ++k) {
+          int d = cs;
+          d = __dp4a(static_cast<int>(e[k][0]), static_cast<int>(xa.x), d);
+          d = __dp4a(static_cast<int>(e[k][1]), static_cast<int>(xa.y), d);
+          d = __dp4a(static_cast<int>(e[k][2]), static_cast<int>(xa.z), d);
+          d = __dp4a(static_cast<int>(e[k][3]), static_cast<int>(xa.w), d);
+          d = __dp4a(static_cast<int>(e[k][4]), static_cast<int>(xb.x), d);
+          d = __dp4a(static_cast<int>(e[k][5]), static_cast<int>(xb.y), d);
+          d = __dp4a(static_cast<int>(e[k][6]), static_cast<int>(xb.z), d);
+          d = __dp4a(static_cast<int>(e[k][7]), static_cast<int>(xb.w), d);
+          acc[k][m] += q[k] * d;
+        }
       }
     }
-    // reduce-scatter over the tokens, then finish the sum of the lane's token
-    int tm = 0;
+    // per row of the group: reduce-scatter over the tokens, then finish the lane's token
 #pragma unroll
-    for (int st = 0; st < T::LOG2MT; ++st) {
-      const int half = MT >> (st + 1);
-      const int o = 16 >> st;
-      const bool up = (lane & o) != 0;
+    for (int k = 0; k < GR; ++k) {
+      int tm = 0;
 #pragma unroll
-      for (int k = 0; k < half; ++k) {
-        const int send = up ? acc[k] : acc[k + half];
-        const int keep = up ? acc[k + half] : acc[k];
-        acc[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      for (int st = 0; st < T::LOG2MT; ++st) {
+        const int half = MT >> (st + 1);
+        const int o = 16 >> st;
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int h = 0; h < half; ++h) {
+          const int send = up ? acc[k][h] : acc[k][h + half];
+          const int keep = up ? acc[k][h + half] : acc[k][h];
+          acc[k][h] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+        if (up) tm += half;
       }
-      if (up) tm += half;
-    }
 #pragma unroll
-    for (int o = 16 >> T::LOG2MT; o > 0; o >>= 1) acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
-    if ((lane & ((32 >> T::LOG2MT) - 1)) == 0 && tm < M) {
-      const int n = n0 + r;
-      const size_t idx = static_cast<size_t>(tm) * N + n;
-      if (acc_dbg != nullptr) acc_dbg[idx] = acc[0];
-      store_y(y, y_dtype, idx, __fmul_rn(__fmul_rn(__int2float_rn(acc[0]), sw[n]), sxs[tm]));
+      for (int o = 16 >> T::LOG2MT; o > 0; o >>= 1) acc[k][0] += __shfl_xor_sync(0xffffffffu, acc[k][0], o);
+      if ((lane & ((32 >> T::LOG2MT) - 1)) == 0 && tm < M) {
+        const int n = n0 + warp + kDecWarps * (g * GR + k);
+        const size_t idx = static_cast<size_t>(tm) * N + n;
+        if (acc_dbg != nullptr) acc_dbg[idx] = acc[k][0];
+        store_y(y, y_dtype, idx, __fmul_rn(__fmul_rn(__int2float_rn(acc[k][0]), sw[n]), sxs[tm]));
+      }
     }
   }
 }
