@@ -120,16 +120,22 @@ __device__ __forceinline__ void stage_q(const int8_t* __restrict__ qT, int N, in
 // ring and 4-row CTAs would leave too few warps per SM for short N (down_proj,
 // K = 17408, N = 5120: 160 CTAs of 32 rows took 10.9 us, 320 of 16 take 8.2 us,
 // 640 of 8 need 1.4 waves at 78 registers and took 10.0 us).
+// While K <= 8192 the ring is one chunk step deep and the registers are capped
+// for 5 CTAs per SM: a layer (544 CTAs at the gate+up shape) then leaves 216
+// CTA slots free, so the next kernel's CTAs become resident and start their
+// weight loads while this one computes (3 steps deep at 4 CTAs per SM, the
+// rotate+GEMV pair took 7.7 us per layer; one step deep at 5 per SM, 7.0 us).
 template <int PL>
 struct M1Traits {
   static constexpr int RPW = PL <= 8 ? 4 : 2;                 // rows per warp
   static constexpr int ROWS = kDecWarps * RPW;                // rows per CTA
-  static constexpr int RC = PL <= 4 ? PL : (PL <= 8 ? 3 : 8);  // chunk steps (of all RPW rows) in flight
+  static constexpr int RC = PL <= 8 ? 1 : 8;                  // chunk steps (of all RPW rows) in flight
+  static constexpr int MIN_CTAS = PL <= 8 ? 5 : 0;            // register cap (0: none)
   static constexpr int QSTRIDE = ROWS + 4;                    // padded q row: conflict-free reads
 };
 
 template <int PL>
-__global__ void __launch_bounds__(kDecWarps * 32)
+__global__ void __launch_bounds__(kDecWarps * 32, M1Traits<PL>::MIN_CTAS)
 decode1_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ qT,
                const float* __restrict__ sw, const int8_t* __restrict__ xq,
                const float* __restrict__ sx, int N, void* __restrict__ y, int y_dtype,
