@@ -18,7 +18,9 @@
 // half-warp. The quantiser is the layer's own:
 // inv = fl32(127 / a), q = clamp(rne(fl32(x inv)), -127, 127), scale =
 // fl32(a / 127); decompression is fl32(q scale) added in fp32 from the own
-// part in peer order, rounded once to bf16.
+// part in peer order, rounded once to bf16. The two IEEE quotients of a group
+// are computed once per warp lane (one lane per quotient), not by all 16 lanes
+// of the group: 6.8 -> 6.3 us at 1584 x 5120.
 #include "tl_internal.cuh"
 
 #include <cuda_bf16.h>
@@ -46,40 +48,73 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return a | (b << 16);
 }
 
+// clamp(rne(v), -127, 127) as one byte, with NaN -> 0 (the value an fp32 ->
+// int conversion gives it): the NaN-propagating max keeps a NaN a NaN, and the
+// saturating conversion turns it into 0 and +inf into 127.
+__device__ __forceinline__ uint32_t code_byte(float v) {
+  float c;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(c) : "f"(v), "f"(-127.f));
+  uint32_t r;
+  asm("cvt.rni.sat.s8.f32 %0, %1;" : "=r"(r) : "f"(c));
+  return r;
+}
+
+// Each thread quantises U vectors of 8 elements; the 2U groups of a warp need
+// 4U IEEE quotients (127 / a and a / 127 per group), one per lane, exchanged by
+// shuffles, instead of 2U per lane.
+template <int U>
 __global__ void __launch_bounds__(kCodecThreads)
 codec_quant_kernel(const uint4* __restrict__ x, size_t nvec, uint2* __restrict__ q,
                    float* __restrict__ scale) {
+  static_assert(4 * U <= 32, "one quotient per lane");
   pdl_wait_prior();   // x is normally the preceding kernel's output
   const int lane = threadIdx.x & 31;
-  const size_t base = static_cast<size_t>(blockIdx.x) * kCodecThreads * kQuantUnroll + threadIdx.x;
-  uint4 v[kQuantUnroll];
+  const size_t base = static_cast<size_t>(blockIdx.x) * kCodecThreads * U + threadIdx.x;
+  uint4 v[U];
 #pragma unroll
-  for (int u = 0; u < kQuantUnroll; ++u) {
+  for (int u = 0; u < U; ++u) {
     const size_t idx = base + static_cast<size_t>(u) * kCodecThreads;
     v[u] = idx < nvec ? __ldcs(x + idx) : make_uint4(0, 0, 0, 0);
   }
   pdl_launch_dependents();
+  float f[U][8], a[U];
 #pragma unroll
-  for (int u = 0; u < kQuantUnroll; ++u) {
+  for (int u = 0; u < U; ++u) {
+    bf16x8_to_f32(v[u], f[u]);
+    a[u] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) a[u] = fmaxf(a[u], fabsf(f[u][e]));
+#pragma unroll
+    for (int o = kVecPerGroup / 2; o > 0; o >>= 1) a[u] = fmaxf(a[u], __shfl_xor_sync(0xffffffffu, a[u], o));
+  }
+  // quotient d = lane mod 4U: group (u, half) = (d >> 2, (d >> 1) & 1), kind d & 1
+  const int d = lane & (4 * U - 1);
+  const int du = d >> 2, dh = (d >> 1) & 1;
+  float ad = 0.f;
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const float t = __shfl_sync(0xffffffffu, a[u], 16 * dh);
+    if (u == du) ad = t;
+  }
+  const bool kind = (d & 1) != 0;
+  const float num = kind ? ad : 127.f, den = kind ? 127.f : ad;
+  const float r = ad > 0.f ? __fdiv_rn(num, den) : 0.f;
+  const int half = lane >> 4;
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
     const size_t idx = base + static_cast<size_t>(u) * kCodecThreads;
-    float f[8];
-    bf16x8_to_f32(v[u], f);
-    float a = 0.f;
+    const int src = 4 * u + 2 * half;
+    const float inv = __shfl_sync(0xffffffffu, r, src);
+    const float sc = __shfl_sync(0xffffffffu, r, src + 1);
+    uint32_t c[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(f[e]));
-#pragma unroll
-    for (int o = kVecPerGroup / 2; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    const float inv = a > 0.f ? __fdiv_rn(127.f, a) : 0.f;
-    const float s = a > 0.f ? __fdiv_rn(a, 127.f) : 0.f;
-    int c[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) c[e] = quant_i8(f[e], inv);
+    for (int e = 0; e < 8; ++e) c[e] = code_byte(__fmul_rn(f[u][e], inv));
     if (idx < nvec) {
       uint2 o;
-      o.x = (c[0] & 0xFF) | ((c[1] & 0xFF) << 8) | ((c[2] & 0xFF) << 16) | ((c[3] & 0xFF) << 24);
-      o.y = (c[4] & 0xFF) | ((c[5] & 0xFF) << 8) | ((c[6] & 0xFF) << 16) | ((c[7] & 0xFF) << 24);
+      o.x = __byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040), 0x5410);
+      o.y = __byte_perm(__byte_perm(c[4], c[5], 0x0040), __byte_perm(c[6], c[7], 0x0040), 0x5410);
       q[idx] = o;
-      if ((lane & (kVecPerGroup - 1)) == 0) scale[idx / kVecPerGroup] = s;
+      if ((lane & (kVecPerGroup - 1)) == 0) scale[idx / kVecPerGroup] = sc;
     }
   }
 }
@@ -149,7 +184,7 @@ cudaError_t launch_dq(const uint16_t* own, const int8_t* q, const float* scale, 
 cudaError_t launch_codec_quant(const uint16_t* x, int R, int H, int8_t* q, float* scale,
                                cudaStream_t st) {
   const size_t nvec = static_cast<size_t>(R) * H / 8;
-  return launch_pdl(codec_quant_kernel, codec_grid(nvec, kQuantUnroll), dim3(kCodecThreads), 0, st,
+  return launch_pdl(codec_quant_kernel<kQuantUnroll>, codec_grid(nvec, kQuantUnroll), dim3(kCodecThreads), 0, st,
                     reinterpret_cast<const uint4*>(x), nvec, reinterpret_cast<uint2*>(q), scale);
 }
 

@@ -366,13 +366,15 @@ __device__ __forceinline__ float rotate_block_warp(const uint16_t* __restrict__ 
   }
 #pragma unroll
   for (int t = 1; t < 32; t <<= 1) {
-    const bool upper = (lane & t) != 0;
+    // o - v on the upper lane of the pair, v + o on the lower: v * (+-1) + o,
+    // exact before its one rounding, so bit for bit the subtract or the add
+    const float sg = (lane & t) != 0 ? -1.f : 1.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float o = __shfl_xor_sync(0xffffffffu, v[j][e], t);
-        v[j][e] = upper ? __fsub_rn(o, v[j][e]) : __fadd_rn(v[j][e], o);
+        v[j][e] = __fmaf_rn(v[j][e], sg, o);
       }
     }
   }
