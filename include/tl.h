@@ -159,8 +159,9 @@ int tl_linear_decode(const uint8_t* packed, const int8_t* qT, const float* sw,
  *   sx_out   optional fp32 [1] receiving the token scale (NULL: not written)
  *   other arguments as for tl_linear_decode. M = 0 is a no-op; M > 1 or
  *   K > 8192 returns TL_EUNSUPPORTED.
- * Every CTA rotates the token itself, so x must be complete when the kernel
- * starts reading it (it waits for the preceding kernel in the stream first).
+ * The token is rotated once per cluster of CTAs, which share it through
+ * distributed shared memory; x must be complete when the kernel starts
+ * reading it (it waits for the preceding kernel in the stream first).
  */
 int tl_linear_decode_fused(const uint8_t* packed, const int8_t* qT, const float* sw,
                            const uint16_t* x, const int8_t* signs, int M, int N, int K, void* y,

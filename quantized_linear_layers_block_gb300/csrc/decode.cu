@@ -134,6 +134,105 @@ struct M1Traits {
   static constexpr int QSTRIDE = ROWS + 4;                    // padded q row: conflict-free reads
 };
 
+// The CTA's shared state of the M = 1 GEMV (as the fused kernel below holds
+// it): the staged, permuted token and q.
+template <int PL>
+struct M1Smem {
+  static constexpr int NC = PL * kBlock / 32;
+  static constexpr int G = PL * kBlock / kGroup;
+  uint4 xw0[NC];
+  uint4 xw1[NC];
+  int csum[NC];
+  int8_t qs[G * M1Traits<PL>::QSTRIDE];
+};
+
+// Entry of an M = 1 CTA: the first RC chunk steps of the warp's rows into the
+// register ring, then q of the CTA's rows (qT is group-major: ROWS contiguous
+// bytes per group). Weights only, so it runs before the wait on the
+// preceding kernel.
+template <int PL>
+__device__ __forceinline__ void m1_prologue(const uint32_t* __restrict__ packed,
+                                            const int8_t* __restrict__ qT, int N, M1Smem<PL>& sm,
+                                            uint2 (&ring)[M1Traits<PL>::RC][M1Traits<PL>::RPW]) {
+  using T = M1Traits<PL>;
+  constexpr int NC = M1Smem<PL>::NC, G = M1Smem<PL>::G;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n0 = blockIdx.x * T::ROWS;
+  const uint2* pw = reinterpret_cast<const uint2*>(packed) + static_cast<size_t>(n0 + warp) * NC + lane;
+  constexpr size_t kRowStep = static_cast<size_t>(kDecWarps) * NC;   // uint2 between a warp's rows
+#pragma unroll
+  for (int i = 0; i < T::RC; ++i) {
+#pragma unroll
+    for (int j = 0; j < T::RPW; ++j) ring[i][j] = __ldg(pw + j * kRowStep + i * 32);
+  }
+  pdl_launch_dependents();
+  for (int i = tid; i < G * (T::ROWS / 4); i += blockDim.x) {
+    const int g = i / (T::ROWS / 4), r4 = i % (T::ROWS / 4);
+    *reinterpret_cast<uint32_t*>(sm.qs + g * T::QSTRIDE + 4 * r4) =
+        *reinterpret_cast<const uint32_t*>(qT + static_cast<size_t>(g) * N + n0 + 4 * r4);
+  }
+}
+
+// The GEMV of the CTA's rows from the staged token, and its epilogue.
+template <int PL>
+__device__ __forceinline__ void m1_gemv(const uint32_t* __restrict__ packed,
+                                        const float* __restrict__ sw, float sx0, int N,
+                                        const M1Smem<PL>& sm,
+                                        uint2 (&ring)[M1Traits<PL>::RC][M1Traits<PL>::RPW],
+                                        void* __restrict__ y, int y_dtype,
+                                        int32_t* __restrict__ acc_dbg) {
+  using T = M1Traits<PL>;
+  constexpr int NC = M1Smem<PL>::NC;
+  constexpr int RPW = T::RPW, RC = T::RC, QS = T::QSTRIDE;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n0 = blockIdx.x * T::ROWS;
+  const uint2* pw = reinterpret_cast<const uint2*>(packed) + static_cast<size_t>(n0 + warp) * NC + lane;
+  constexpr size_t kRowStep = static_cast<size_t>(kDecWarps) * NC;
+  int acc[RPW];
+#pragma unroll
+  for (int k = 0; k < RPW; ++k) acc[k] = 0;
+#pragma unroll
+  for (int i = 0; i < PL; ++i) {
+    const int c = i * 32 + lane;
+    const uint4 xa = sm.xw0[c], xb = sm.xw1[c];      // read once for all the warp's rows
+    const int cs = -sm.csum[c];
+    const int8_t* qrow = sm.qs + (8 * i + (lane >> 2)) * QS + warp;
+#pragma unroll
+    for (int k = 0; k < RPW; ++k) {
+      const uint2 wv = ring[i % RC][k];
+      if (i + RC < PL) ring[i % RC][k] = __ldg(pw + k * kRowStep + (i + RC) * 32);
+      const int t = dot_chunk2(wv.x, wv.y, xa, xb, cs);
+      acc[k] += static_cast<int>(qrow[kDecWarps * k]) * t;
+    }
+  }
+  // the RPW sums together: exchange halves, then the remaining butterfly steps
+  int tk = 0;
+  constexpr int LOG2R = RPW == 1 ? 0 : (RPW == 2 ? 1 : 2);
+#pragma unroll
+  for (int st = 0; st < LOG2R; ++st) {
+    const int half = RPW >> (st + 1);
+    const int o = 16 >> st;
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < half; ++k) {
+      const int send = up ? acc[k] : acc[k + half];
+      const int keep = up ? acc[k + half] : acc[k];
+      acc[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+    if (up) tk += half;
+  }
+#pragma unroll
+  for (int o = 16 >> LOG2R; o > 0; o >>= 1) acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
+  if ((lane & ((32 >> LOG2R) - 1)) == 0) {
+    const int n = n0 + warp + kDecWarps * tk;
+    if (acc_dbg != nullptr) acc_dbg[n] = acc[0];
+    store_y(y, y_dtype, n, __fmul_rn(__fmul_rn(__int2float_rn(acc[0]), sw[n]), sx0));
+  }
+}
+
+// decode1_kernel keeps its own copy of the prologue and the GEMV: built from
+// the shared functions above it measured 4 % slower back to back (5.37 against
+// 5.15 us at the gate+up shape), with the same results.
 template <int PL>
 __global__ void __launch_bounds__(kDecWarps * 32, M1Traits<PL>::MIN_CTAS)
 decode1_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ qT,
@@ -380,82 +479,73 @@ decodem_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ q
 }
 
 // ---------------------------------------------------------------- M = 1, fused
-// One launch for the whole layer at M = 1: the kernel takes the bf16 token,
-// and every CTA performs the input-side rotation and the per-token
-// quantisation itself (one warp per 1024-block, the same arithmetic as
-// tl_rotate_quant_act) before the GEMV. To keep that redundant rotation rare
-// the grid is one 1024-thread CTA per SM: CTA c owns a balanced, contiguous
-// range of 4-row quads (at most 32, one per warp), so each SM rotates the token
-// once. The dot product takes two masks per packed word instead of four
-// shift-and-mask pairs (fields 0 and 2 at scale 1, fields 1 and 3 at scale 4:
-// sum = P + Q/4, exact since Q is a multiple of 4), and a warp reduces its four
-// row sums together (two exchange steps that halve the rows, then three
-// butterfly steps).
+// One launch for the whole layer at M = 1: the kernel takes the bf16 token and
+// does the input-side rotation and the per-token quantisation itself (the
+// arithmetic of tl_rotate_quant_act, so the result is the same bit for bit)
+// before the M = 1 GEMV above (same rows per CTA, same register cap). The
+// grid runs in clusters of CS CTAs that share the token through distributed
+// shared memory: warp w of cluster rank r rotates block b = w CS + r, pushes
+// the block maximum to every CTA of the cluster, and after a cluster barrier
+// quantises its block, permutes it into the dp4a order (one chunk per lane)
+// and pushes the chunks and their sums to every CTA of the cluster; a second
+// barrier and the GEMV follows. So a token is rotated once per cluster, by
+// CTAs that would otherwise wait, and no CTA reads a peer after the second
+// barrier (each one's shared memory outlives every write into it). The
+// registers are capped for 4 CTAs per SM, not 5: under the 48-register cap
+// the rotation spills, and its local loads queue behind the weight stream
+// (10.2 us per layer against 8.0 at 64 registers). The rotation stays on the
+// critical path of every layer, so the two-launch rotate + GEMV pair remains
+// faster (7.2-7.4 us); clusters of 1, 2, 4 or 8 CTAs measured the same.
 
-constexpr int kFusedWarps = 32;
-constexpr int kFusedMaxQuads = kFusedWarps;
-constexpr int kFusedQStride = 4 * (kFusedMaxQuads + 1);   // odd word count: conflict-free q reads
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_peer(uint32_t a, uint4 v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ void st_peer(uint32_t a, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_peer(uint32_t a, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
 
-template <int PL>
-__global__ void __launch_bounds__(kFusedWarps * 32, 1)
+template <int PL, int CS>
+__global__ void __launch_bounds__(kDecWarps * 32, 4)
 decode1f_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ qT,
                 const float* __restrict__ sw, const uint16_t* __restrict__ x,
                 const int8_t* __restrict__ signs, int N, void* __restrict__ y, int y_dtype,
                 int32_t* __restrict__ acc_dbg, int8_t* __restrict__ xq_out,
                 float* __restrict__ sx_out) {
-  constexpr int K = PL * kBlock;
-  constexpr int G = K / kGroup;
-  constexpr int NC = K / 32;
-  // rows of weights in flight per warp; the rotation's 32 values per lane share the registers
-  constexpr int RR = PL <= 2 ? 4 : (PL <= 5 ? 2 : 1);
-  __shared__ __align__(16) uint4 xw0[NC];
-  __shared__ __align__(16) uint4 xw1[NC];
-  __shared__ int csum[NC];
-  __shared__ __align__(16) int8_t xnat[K];              // quantised token, natural order
+  static_assert(PL <= kDecWarps * CS, "one rotating warp per block");
+  __shared__ __align__(16) M1Smem<PL> sm;
+  __shared__ __align__(16) int8_t xnat[kDecWarps][kBlock];   // a rotating warp's quantised block
   __shared__ float bmax[PL];
-  __shared__ __align__(16) int8_t qs[G * kFusedQStride];  // q of the CTA's rows, [group][row]
-
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const int warp = tid >> 5;
-  const int Q = N >> 2;
-  const int q0 = static_cast<int>(static_cast<long long>(blockIdx.x) * Q / gridDim.x);
-  const int nq = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * Q / gridDim.x) - q0;
-  const int nb = 4 * q0;                                 // first row of the CTA
-  const int j = warp;                                    // this warp's quad
-  const uint2* pq = reinterpret_cast<const uint2*>(packed) + static_cast<size_t>(nb + 4 * j) * NC + lane;
-
-  uint2 ring[RR][PL];
-  if (j < nq) {
-#pragma unroll
-    for (int r = 0; r < RR; ++r) {
-#pragma unroll
-      for (int i = 0; i < PL; ++i) ring[r][i] = __ldg(pq + r * NC + i * 32);
-    }
-  }
-  pdl_launch_dependents();
-  for (int i = tid; i < G * nq; i += blockDim.x) {
-    const int g = i / nq, jq = i - g * nq;
-    *reinterpret_cast<uint32_t*>(qs + g * kFusedQStride + 4 * jq) =
-        __ldg(reinterpret_cast<const uint32_t*>(qT + static_cast<size_t>(g) * N + nb + 4 * jq));
-  }
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint2 ring[M1Traits<PL>::RC][M1Traits<PL>::RPW];
+  m1_prologue<PL>(packed, qT, N, sm, ring);
   pdl_wait_prior();
 
+  const uint32_t rank = cluster_ctarank();
+  const int b = warp * CS + static_cast<int>(rank);     // the block this warp rotates, if b < PL
   float v[4][8];
-  if (warp < PL) {
-    float am = rotate_block_warp(x + warp * kBlock, signs == nullptr ? nullptr : signs + warp * kBlock,
-                                 lane, v);
+  if (b < PL) {
+    float am = rotate_block_warp(x + b * kBlock, signs == nullptr ? nullptr : signs + b * kBlock, lane, v);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-    if (lane == 0) bmax[warp] = am;
+    if (lane < CS) st_peer(peer_addr(&bmax[b], lane), am);
   }
-  __syncthreads();
+  cluster_sync();
   float a = 0.f;
 #pragma unroll
-  for (int b = 0; b < PL; ++b) a = fmaxf(a, bmax[b]);
+  for (int i = 0; i < PL; ++i) a = fmaxf(a, bmax[i]);
   const float inv = a > 0.f ? __fdiv_rn(127.f, a) : 0.f;
   const float sx0 = a > 0.f ? __fdiv_rn(a, 127.f) : 0.f;
-  if (warp < PL) {
+  if (b < PL) {
+    const bool out = xq_out != nullptr && blockIdx.x < CS;   // the first cluster writes xq_out
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
       int q8[8];
@@ -464,51 +554,24 @@ decode1f_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ 
       uint2 o;
       o.x = (q8[0] & 0xFF) | ((q8[1] & 0xFF) << 8) | ((q8[2] & 0xFF) << 16) | ((q8[3] & 0xFF) << 24);
       o.y = (q8[4] & 0xFF) | ((q8[5] & 0xFF) << 8) | ((q8[6] & 0xFF) << 16) | ((q8[7] & 0xFF) << 24);
-      const int off = warp * kBlock + 256 * jj + 8 * lane;
-      *reinterpret_cast<uint2*>(xnat + off) = o;
-      if (xq_out != nullptr && blockIdx.x == 0) *reinterpret_cast<uint2*>(xq_out + off) = o;
+      *reinterpret_cast<uint2*>(&xnat[warp][256 * jj + 8 * lane]) = o;
+      if (out) *reinterpret_cast<uint2*>(xq_out + b * kBlock + 256 * jj + 8 * lane) = o;
+    }
+    __syncwarp();
+    const uint4* src = reinterpret_cast<const uint4*>(&xnat[warp][32 * lane]);
+    uint4 p0, p1;
+    const int cs = permute_chunk(src[0], src[1], p0, p1);
+    const int c = b * 32 + lane;                          // chunk of the token
+#pragma unroll
+    for (int r = 0; r < CS; ++r) {
+      st_peer(peer_addr(&sm.xw0[c], r), p0);
+      st_peer(peer_addr(&sm.xw1[c], r), p1);
+      st_peer(peer_addr(&sm.csum[c], r), cs);
     }
   }
   if (sx_out != nullptr && blockIdx.x == 0 && tid == 0) sx_out[0] = sx0;
-  __syncthreads();
-  for (int c = tid; c < NC; c += blockDim.x) {
-    const uint4* src = reinterpret_cast<const uint4*>(xnat + 32 * c);
-    uint4 p0, p1;
-    csum[c] = permute_chunk(src[0], src[1], p0, p1);
-    xw0[c] = p0;
-    xw1[c] = p1;
-  }
-  __syncthreads();
-  if (j >= nq) return;
-
-  int acc[4];
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    int t_acc = 0;
-#pragma unroll
-    for (int i = 0; i < PL; ++i) {
-      const int c = i * 32 + lane;
-      const uint2 wv = ring[r % RR][i];
-      if (r + RR < 4) ring[r % RR][i] = __ldg(pq + (r + RR) * NC + i * 32);
-      const int t = dot_chunk2(wv.x, wv.y, xw0[c], xw1[c], -csum[c]);
-      t_acc += static_cast<int>(qs[(8 * i + (lane >> 2)) * kFusedQStride + 4 * j + r]) * t;
-    }
-    acc[r] = t_acc;
-  }
-  // lanes with bit 4 clear keep rows 0, 1 and those with it set rows 2, 3; then
-  // bit 3 picks one of the two; lanes 0, 8, 16, 24 end with rows 0, 1, 2, 3.
-  const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0;
-  const int s0 = (b4 ? acc[2] : acc[0]) + __shfl_xor_sync(0xffffffffu, b4 ? acc[0] : acc[2], 16);
-  const int s1 = (b4 ? acc[3] : acc[1]) + __shfl_xor_sync(0xffffffffu, b4 ? acc[1] : acc[3], 16);
-  int s = (b3 ? s1 : s0) + __shfl_xor_sync(0xffffffffu, b3 ? s0 : s1, 8);
-  s += __shfl_xor_sync(0xffffffffu, s, 4);
-  s += __shfl_xor_sync(0xffffffffu, s, 2);
-  s += __shfl_xor_sync(0xffffffffu, s, 1);
-  if ((lane & 7) == 0) {
-    const int n = nb + 4 * j + 2 * (lane >> 4) + ((lane >> 3) & 1);
-    if (acc_dbg != nullptr) acc_dbg[n] = s;
-    store_y(y, y_dtype, n, __fmul_rn(__fmul_rn(__int2float_rn(s), sw[n]), sx0));
-  }
+  cluster_sync();
+  m1_gemv<PL>(packed, sw, sx0, N, sm, ring, y, y_dtype, acc_dbg);
 }
 
 // ---------------------------------------------------------------- 1 <= M <= 32
@@ -725,19 +788,26 @@ int try_mm(const uint32_t* packed, const int8_t* qT, const float* sw, const int8
   }
 }
 
+template <int PL, int CS>
+cudaError_t launch_m1f_cs(const uint32_t* packed, const int8_t* qT, const float* sw, const uint16_t* x,
+                          const int8_t* signs, int N, void* y, int y_dtype, int32_t* acc_dbg,
+                          int8_t* xq_out, float* sx_out, cudaStream_t st) {
+  return launch_pdl_cluster(decode1f_kernel<PL, CS>, dim3(N / M1Traits<PL>::ROWS), dim3(kDecWarps * 32), 0,
+                            st, CS, packed, qT, sw, x, signs, N, y, y_dtype, acc_dbg, xq_out, sx_out);
+}
+
+// Clusters of 8 CTAs where the grid allows it, else 4 (N is a multiple of 128,
+// so the grid N / 32 always is a multiple of 4).
 template <int PL>
 cudaError_t launch_m1f(const uint32_t* packed, const int8_t* qT, const float* sw, const uint16_t* x,
                        const int8_t* signs, int N, void* y, int y_dtype, int32_t* acc_dbg,
                        int8_t* xq_out, float* sx_out, cudaStream_t st) {
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  const int quads = N / 4;
-  int grid = (quads + kFusedMaxQuads - 1) / kFusedMaxQuads;   // at most 32 quads per CTA
-  if (grid < sms) grid = sms < quads ? sms : quads;
-  return launch_pdl(decode1f_kernel<PL>, dim3(grid), dim3(kFusedWarps * 32), 0, st, packed, qT, sw,
-                    x, signs, N, y, y_dtype, acc_dbg, xq_out, sx_out);
+  const int grid = N / M1Traits<PL>::ROWS;
+  if (grid % 8 == 0)
+    return launch_m1f_cs<PL, 8>(packed, qT, sw, x, signs, N, y, y_dtype, acc_dbg, xq_out, sx_out, st);
+  if (grid % 4 == 0)
+    return launch_m1f_cs<PL, 4>(packed, qT, sw, x, signs, N, y, y_dtype, acc_dbg, xq_out, sx_out, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
