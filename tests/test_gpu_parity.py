@@ -215,6 +215,22 @@ def test_decode_fused_matches_two_step(tl, K, signed):
         _compare(L, acc1.cpu().numpy(), y1, 4)
 
 
+@pytest.mark.parametrize("K", [1024, 5120, 8192])
+def test_decode_fused_clusters_of_four(tl, K):
+    """N / 32 not a multiple of 8 (N = 384: 12 CTAs) runs the fused kernel in clusters of 4."""
+    L = synth.config_inputs("decode", M=1, N=384, K=K)
+    packed, qT, sw = pack_dev(tl, L)
+    x = x_dev(L)
+    acc2 = torch.empty((1, L.N), dtype=torch.int32, device="cuda")
+    xq, sx = tl.tl_rotate_quant_act(x, xq_dtype=tl.TL_I8)
+    y2 = tl.tl_linear_decode(packed, qT, sw, xq, sx, L.N, L.K, 4, acc_dbg=acc2)
+    acc1 = torch.full((1, L.N), ACC_SENTINEL, dtype=torch.int32, device="cuda")
+    y1 = tl.tl_linear_decode_fused(packed, qT, sw, x, L.N, L.K, 4, acc_dbg=acc1)
+    check_status(tl)
+    assert torch.equal(acc1, acc2) and torch.equal(y1, y2)
+    _compare(L, acc1.cpu().numpy(), y1, 4)
+
+
 def test_decode_fused_full_size(tl):
     L = synth.config_inputs("decode")
     packed, qT, sw = pack_dev(tl, L)
