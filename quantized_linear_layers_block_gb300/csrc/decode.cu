@@ -125,12 +125,14 @@ __device__ __forceinline__ void stage_q(const int8_t* __restrict__ qT, int N, in
 // CTA slots free, so the next kernel's CTAs become resident and start their
 // weight loads while this one computes (3 steps deep at 4 CTAs per SM, the
 // rotate+GEMV pair took 7.7 us per layer; one step deep at 5 per SM, 7.0 us).
+// CTAs per SM the M = 1 kernel's registers are capped for (0: no cap)
+__host__ __device__ constexpr int m1_min_ctas(int pl) { return pl <= 8 ? 5 : 0; }
+
 template <int PL>
 struct M1Traits {
   static constexpr int RPW = PL <= 8 ? 4 : 2;                 // rows per warp
   static constexpr int ROWS = kDecWarps * RPW;                // rows per CTA
   static constexpr int RC = PL <= 8 ? 1 : 8;                  // chunk steps (of all RPW rows) in flight
-  static constexpr int MIN_CTAS = PL <= 8 ? 5 : 0;            // register cap (0: none)
   static constexpr int QSTRIDE = ROWS + 4;                    // padded q row: conflict-free reads
 };
 
@@ -234,7 +236,7 @@ __device__ __forceinline__ void m1_gemv(const uint32_t* __restrict__ packed,
 // the shared functions above it measured 4 % slower back to back (5.37 against
 // 5.15 us at the gate+up shape), with the same results.
 template <int PL>
-__global__ void __launch_bounds__(kDecWarps * 32, M1Traits<PL>::MIN_CTAS)
+__global__ void __launch_bounds__(kDecWarps * 32, m1_min_ctas(PL))
 decode1_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ qT,
                const float* __restrict__ sw, const int8_t* __restrict__ xq,
                const float* __restrict__ sx, int N, void* __restrict__ y, int y_dtype,
