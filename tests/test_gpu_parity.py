@@ -327,6 +327,29 @@ def test_exactness_adversarial(tl):
         assert np.array_equal(acc.astype(np.int64), r["acc"])
 
 
+def test_exactness_largest_accumulator(tl):
+    """K = 32768 with every term at +-127*127: |acc| = 127*127*32768 = 528,515,072, the largest
+    the layer can produce (below 2^31). x = 2.0 at channel 0 of every block gives xq = 127
+    everywhere (as above); row 0 all +1, row 1 all -1, row 2 the sign flipping every block,
+    the rest random."""
+    K, N, M = 32768, 128, 1
+    x = np.zeros((M, K), dtype=np.float32)
+    x[:, 0::1024] = 2.0
+    codes = np.random.default_rng(6).integers(-1, 2, size=(N, K)).astype(np.int8)
+    codes[0] = 1
+    codes[1] = -1
+    codes[2] = np.repeat(np.where(np.arange(K // 1024) % 2 == 0, 1, -1), 1024)
+    s = np.full((N, K // 128), 2.0 ** -4, dtype=np.float16)
+    L = synth.LayerInputs(codes=codes, s=s, x_bits=synth.bf16_bits_from_f32(x))
+    packed, qT, sw = pack_dev(tl, L)
+    r = O.layer(L.x_bits, L.codes, L.s)
+    assert int(r["acc"][0, 0]) == 127 * 127 * K and int(r["acc"][0, 1]) == -127 * 127 * K
+    assert int(r["acc"][0, 2]) == 0
+    for path in ("prefill", "decode"):
+        acc, y = _run(tl, path, L, packed, qT, sw, 4)
+        assert np.array_equal(acc.astype(np.int64), r["acc"]), path
+
+
 def test_bounded_inputs_extreme_values(tl):
     """Saturated scales and activations at bf16 range edges stay exact."""
     rng = np.random.default_rng(77)
@@ -347,6 +370,17 @@ def test_bounded_inputs_extreme_values(tl):
 
 
 # ------------------------------------------------------------------ full-size workloads, sampled rows
+
+@pytest.mark.parametrize("path,M", [("decode", 1), ("decode", 5), ("decode", 32),
+                                    ("prefill", 1), ("prefill", 160)])
+def test_largest_k(tl, path, M):
+    """K = 32768, the largest the library takes: the one-CTA-per-token rotation runs 1024 threads,
+    decode takes its generic K path (and slabs at M = 32), |acc| may reach 127 * 127 * 32768."""
+    L = synth.config_inputs("decode", M=M, N=256, K=32768)
+    packed, qT, sw = pack_dev(tl, L)
+    acc, y = _run(tl, path, L, packed, qT, sw, 4)
+    _compare(L, acc, y, 4, frobenius=False)
+
 
 def _sample_rows(N, n=192, seed=0):
     rng = np.random.default_rng(seed)
