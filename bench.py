@@ -172,6 +172,43 @@ def oracle_rate(kind: str, budget_s: float, min_reps: int = 1, M_s=None, N_s=Non
     return rate, unit, sample, reps, el, threads
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
+def oracle_rate_1core(kind: str, budget_s: float):
+    """oracle_rate on the same sample in a fresh interpreter whose BLAS and OpenMP pools have one
+    thread (the pools are sized when numpy loads, so this needs its own process). Returns the
+    rate, or None if the child failed."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", VECLIB_MAXIMUM_THREADS="1")
+    code = ("import json, bench; r = bench.oracle_rate(%r, %r); print(json.dumps([r[0], r[5]]))"
+            % (kind, budget_s))
+    try:
+        out = subprocess.run([sys.executable, "-c", code], env=env, cwd=ROOT, capture_output=True,
+                             text=True, timeout=600)
+        rate, threads = json.loads(out.stdout.strip().splitlines()[-1])
+        return rate if threads == 1 else None
+    except Exception:
+        return None
+
+
 def reference_main(args):
     ws, rank, _ = dist_info()
     if rank != 0:
@@ -496,10 +533,12 @@ def main(argv=None):
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         rate, unit, sample, _, _, threads = oracle_rate("prefill", 10.0)
         line["cpu_baseline"] = {"value": rate, "unit": unit, "cores": threads, "kind": "oracle",
-                                "sample": sample}
+                                "sample": sample, "cpu": cpu_model(),
+                                "value_1core": oracle_rate_1core("prefill", 10.0)}
         drate, dunit, dsample, _, _, _ = oracle_rate("decode", 5.0)
         line["decode"]["cpu_baseline"] = {"value": drate, "unit": dunit, "cores": threads,
-                                          "kind": "oracle", "sample": dsample}
+                                          "kind": "oracle", "sample": dsample,
+                                          "value_1core": oracle_rate_1core("decode", 5.0)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     reps_.close()
