@@ -198,13 +198,12 @@ def oracle_rate_1core(kind: str, budget_s: float):
     rate, or None if the child failed."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                BLIS_NUM_THREADS="1", VECLIB_MAXIMUM_THREADS="1")
-    code = ("import json, bench; r = bench.oracle_rate(%r, %r); print(json.dumps([r[0], r[5]]))"
+    code = ("import json, bench; r = bench.oracle_rate(%r, %r); print(json.dumps(r[0]))"
             % (kind, budget_s))
     try:
         out = subprocess.run([sys.executable, "-c", code], env=env, cwd=ROOT, capture_output=True,
                              text=True, timeout=600)
-        rate, threads = json.loads(out.stdout.strip().splitlines()[-1])
-        return rate if threads == 1 else None
+        return float(json.loads(out.stdout.strip().splitlines()[-1]))
     except Exception:
         return None
 
