@@ -47,6 +47,7 @@ CONFIG = {
     "layers_per_step": LAYERS,
     "l2": "inputs larger than L2: 64 distinct layer buffers (2.95 GB prefill, 1.47 GB decode weights)",
 }
+DP4A_PER_CLK_SM = 60.0    # dp4a lane-ops per clock per SM, measured on GB300 (independent chains)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -342,6 +343,24 @@ def main(argv=None):
         lay, x, y = dec_layers[li]
         tl.tl_linear_decode_fused(lay.packed, lay.qT, lay.sw, x, D["N"], D["K"], tl.TL_BF16, y=y)
 
+    # M = 16 at the decode shape: the whole layer as TernaryLinear runs it (M*K > 72K: K1 with
+    # the fp16 image, then the tensor-core kernel), and that kernel alone
+    M16 = 16
+    _, _, x16 = synth.torch_config_layer(D["name"], 0, M=M16, device=str(dev))
+    y16 = torch.empty((M16, D["N"]), dtype=torch.bfloat16, device=dev)
+    xq16 = torch.empty((M16, D["K"]), dtype=torch.float16, device=dev)
+    sx16 = torch.empty((M16,), dtype=torch.float32, device=dev)
+    ws16 = dec_layers[0][0]._workspace(M16)
+    tl.tl_rotate_quant_act(x16, xq_dtype=tl.TL_F16, xq=xq16, sx=sx16)
+
+    def layer16(li):
+        dec_layers[li][0].forward(x16, out=y16)
+
+    def kernel16(li):
+        lay = dec_layers[li][0]
+        tl.tl_linear_prefill(lay.packed, lay.qT, lay.sw, xq16, sx16, D["N"], D["K"], tl.TL_BF16,
+                             y=y16, workspace=ws16)
+
     # warm-up (also resolves driver entry points and kernel attributes before capture)
     for _ in range(args.warmup):
         for li in range(LAYERS):
@@ -372,12 +391,25 @@ def main(argv=None):
     with torch.cuda.graph(g_df, capture_error_mode="relaxed"):
         for li in range(LAYERS):
             decode_fused(li)
+    g_16 = torch.cuda.CUDAGraph()
+    g_16k = torch.cuda.CUDAGraph()
+    for li in range(LAYERS):
+        layer16(li)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g_16, capture_error_mode="relaxed"):
+        for li in range(LAYERS):
+            layer16(li)
+    with torch.cuda.graph(g_16k, capture_error_mode="relaxed"):
+        for li in range(LAYERS):
+            kernel16(li)
     for _ in range(args.warmup):
         g_dec.replay()
         g_dk.replay()
         g_df.replay()
         g_ff.replay()
         g_fk.replay()
+        g_16.replay()
+        g_16k.replay()
     torch.cuda.synchronize()
     if tl.tl_get_status() != tl.TL_OK:
         raise RuntimeError("device status after warm-up")
@@ -433,6 +465,8 @@ def main(argv=None):
     fused_us = graph_us(g_df, reps)
     f32_layer_us = graph_us(g_ff, reps)
     f32_kernel_us = graph_us(g_fk, reps)
+    m16_layer_us = graph_us(g_16, reps)
+    m16_kernel_us = graph_us(g_16k, reps)
     status = tl.tl_get_status()
     if status != tl.TL_OK:
         raise RuntimeError(f"device status after timing: {tl.tl_strerror(status)}")
@@ -488,6 +522,9 @@ def main(argv=None):
     dec_alg_bytes = wb + D["M"] * D["K"] + 4 * D["M"] + 2 * D["M"] * D["N"]
     k2_gbs = dec_alg_bytes / (k2_ms * 1e-3) / 1e9
     traffic = _profiled_traffic()
+    flop16 = 2.0 * 16 * D["N"] * D["K"]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_peak = 8 * DP4A_PER_CLK_SM * sms * float(clk.get("sm_mhz") or 2070.0) * 1e6 / 1e12
 
     line = {
         "metric": METRIC, "value": tops, "unit": "TOPS", "n_gpus": ws, "steps": K,
@@ -516,6 +553,19 @@ def main(argv=None):
         "e2e": {"value": ws * e2e_steps * LAYERS * flop_layer / e2e_pre_s / 1e12, "unit": "TOPS",
                 "h2d_bytes_per_step": LAYERS * P["M"] * P["K"] * 2,
                 "d2h_bytes_per_step": LAYERS * P["M"] * P["N"] * 2},
+        "decode16": {
+            "metric": "ternary linear int8 TOPS @M=16, decode shape (K=5120, N=17408)",
+            "value": flop16 / (m16_layer_us * 1e-6) / 1e12, "unit": "TOPS",
+            "layer_us": m16_layer_us, "kernel_us": m16_kernel_us,
+            "kernel": "prefill_kernel (K3), TernaryLinear's choice for M*K > 72K; 64 layer buffers "
+                      "in a CUDA graph",
+            "roofline": {"bound": "alu", "achieved": flop16 / (m16_kernel_us * 1e-6) / 1e12,
+                         "peak": alu_peak, "unit": "TOPS",
+                         "frac": flop16 / (m16_kernel_us * 1e-6) / 1e12 / alu_peak,
+                         "peak_source": "the dp4a decode path's ceiling: 60 dp4a lane-ops per clock "
+                                        "per SM (measured with a probe of independent dp4a chains) "
+                                        "x 8 int8 ops x SMs x the median SM clock sampled here"},
+        },
         "decode_f32act": {
             "metric": "float-activation decode GEMV weight-stream GB/s @M=1",
             "layer_us": f32_layer_us, "kernel_us": f32_kernel_us,
