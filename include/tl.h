@@ -148,18 +148,21 @@ int tl_linear_decode(const uint8_t* packed, const int8_t* qT, const float* sw,
                      void* y, int y_dtype, int32_t* acc_dbg, void* stream);
 
 /*
- * Decode of one token (M = 1) with the input-side rotation and per-token
- * quantisation done inside the GEMV kernel: equivalent, bit for bit, to
- * tl_rotate_quant_act(x, TL_I8) followed by tl_linear_decode, in one launch
- * (Qiita item ecc183fae033565af7cb: 前提 for the rotation, §4 for the per-token
- * int8 and the row/token rescale, §5 for the dp4a decode GEMV).
+ * Decode with the input-side rotation and per-token quantisation done inside
+ * the GEMV kernel: equivalent, bit for bit, to tl_rotate_quant_act(x, TL_I8)
+ * followed by tl_linear_decode, in one launch (Qiita item
+ * ecc183fae033565af7cb: 前提 for the rotation, §4 for the per-token int8 and the
+ * row/token rescale, §5 for the dp4a decode GEMV).
  *
- *   x        bf16 bit patterns [1, K], K <= 8192; signs optional int8 [K] (+1/-1)
- *   xq_out   optional int8 [K] receiving the quantised token (NULL: not written)
- *   sx_out   optional fp32 [1] receiving the token scale (NULL: not written)
- *   other arguments as for tl_linear_decode. M = 0 is a no-op; M > 1 or
- *   K > 8192 returns TL_EUNSUPPORTED.
- * The token is rotated once per cluster of CTAs, which share it through
+ *   x        bf16 bit patterns [M, K]; signs optional int8 [K] (+1/-1)
+ *   xq_out   optional int8 [M, K] receiving the quantised tokens (NULL: not written)
+ *   sx_out   optional fp32 [M] receiving the token scales (NULL: not written)
+ *   other arguments as for tl_linear_decode. M = 0 is a no-op. Supported:
+ *   M = 1 with K <= 8192; 2 <= M <= 16 with M' * K <= 73728, M' = M rounded
+ *   up to a power of two, and K / 1024 in {1, 2, 3, 4, 5, 8, 16, 17} (the
+ *   multi-token decode kernel's shapes: 5 and 8 for M' <= 8, 16 and 17 for
+ *   M' <= 4); anything else returns TL_EUNSUPPORTED and launches nothing.
+ * The tokens are rotated once per cluster of CTAs, which share them through
  * distributed shared memory; x must be complete when the kernel starts
  * reading it (it waits for the preceding kernel in the stream first).
  */

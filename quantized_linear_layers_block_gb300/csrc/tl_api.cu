@@ -197,14 +197,22 @@ int tl_linear_decode_fused(const uint8_t* packed, const int8_t* qT, const float*
                            void* stream) {
   int r = check_linear(packed, qT, sw, x, sw, M, N, K, y, y_dtype, acc_dbg);
   if (r != TL_OK) return r;
-  if (M > 1 || K > tl::kMaxFusedDecodeK) return TL_EUNSUPPORTED;
+  if (M > 16 || (M == 1 && K > tl::kMaxFusedDecodeK)) return TL_EUNSUPPORTED;
   if (M == 0 || N == 0) return TL_OK;
   if ((signs && !aligned16(signs)) || (xq_out && !aligned16(xq_out)) || (sx_out && !aligned16(sx_out)))
     return TL_EINVAL;
-  return tl::launch_decode_fused(reinterpret_cast<const uint32_t*>(packed), qT, sw, x, signs, N, K,
-                                 y, y_dtype, acc_dbg, xq_out, sx_out, as_stream(stream)) == cudaSuccess
-             ? TL_OK
-             : TL_ECUDA;
+  if (M == 1)
+    return tl::launch_decode_fused(reinterpret_cast<const uint32_t*>(packed), qT, sw, x, signs, N,
+                                   K, y, y_dtype, acc_dbg, xq_out, sx_out,
+                                   as_stream(stream)) == cudaSuccess
+               ? TL_OK
+               : TL_ECUDA;
+  bool supported = false;
+  const cudaError_t e = tl::launch_decode_fused_m(reinterpret_cast<const uint32_t*>(packed), qT, sw,
+                                                  x, signs, M, N, K, y, y_dtype, acc_dbg, xq_out,
+                                                  sx_out, as_stream(stream), &supported);
+  if (!supported) return TL_EUNSUPPORTED;
+  return e == cudaSuccess ? TL_OK : TL_ECUDA;
 }
 
 int tl_rotate_act(const uint16_t* x, int M, int K, const int8_t* signs, float* xr, void* stream) {

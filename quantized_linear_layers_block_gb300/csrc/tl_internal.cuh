@@ -56,12 +56,19 @@ cudaError_t launch_rotate_quant(const uint16_t* x, int M, int K, const int8_t* s
 cudaError_t launch_decode(const uint32_t* packed, const int8_t* qT, const float* sw,
                           const int8_t* xq, const float* sx, int M, int N, int K, void* y,
                           int y_dtype, int32_t* acc_dbg, cudaStream_t st);
+// Fused decode of 2 <= M <= 16 tokens (M rounded up to MT, MT * K <= 72 K, the
+// multi-token kernel's K); *supported is false, and nothing is launched, otherwise.
+cudaError_t launch_decode_fused_m(const uint32_t* packed, const int8_t* qT, const float* sw,
+                                  const uint16_t* x, const int8_t* signs, int M, int N, int K,
+                                  void* y, int y_dtype, int32_t* acc_dbg, int8_t* xq_out,
+                                  float* sx_out, cudaStream_t st, bool* supported);
 // M = 1 decode with the rotation and quantisation of x done in each CTA (K <= 8192).
 cudaError_t launch_decode_fused(const uint32_t* packed, const int8_t* qT, const float* sw,
                                 const uint16_t* x, const int8_t* signs, int N, int K, void* y,
                                 int y_dtype, int32_t* acc_dbg, int8_t* xq_out, float* sx_out,
                                 cudaStream_t st);
 constexpr int kMaxFusedDecodeK = 8192;
+constexpr long long kMaxFusedMK = 72 * 1024;   // fused decode of M >= 2 tokens: MT * K staged
 constexpr int kMaxCodecPeers = 7;
 constexpr int kMaxF32ActM = 4;            // tokens of the float-activation decode
 constexpr int kMaxF32ActMK = 36864;       // M * K bound: the staged fp32 activations fit shared memory

@@ -207,7 +207,8 @@ def tl_linear_decode_fused(packed, qT, sw, x, N: int, K: int, y_dtype: int = TL_
                            signs=None, y: torch.Tensor | None = None,
                            acc_dbg: torch.Tensor | None = None, xq_out: torch.Tensor | None = None,
                            sx_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """One token (x bf16 [1,K]) through rotation, quantisation and the decode GEMV in one launch."""
+    """Up to 16 tokens (x bf16 [M, K]) through rotation, quantisation and the decode GEMV in one
+    launch (shapes as tl.h states)."""
     _dev_tensor(x, torch.bfloat16, "x")
     M = x.shape[0]
     y = _linear_out(M, N, y_dtype, x.device, y)

@@ -67,6 +67,14 @@ def test_argument_errors_without_gpu(lib):
     assert lib.tl_linear_prefill(ok, ok, ok, ok, ok, 1, 128, 1000, ok, tl.TL_F32, None, None, 0, None) == tl.TL_EUNSUPPORTED
     assert lib.tl_linear_prefill(ok, ok, ok, ok, ok, 1, 128, 33792, ok, tl.TL_F32, None, None, 0, None) == tl.TL_EUNSUPPORTED
     assert lib.tl_rotate_quant_act(ok, 1, 1536, None, ok, tl.TL_I8, ok, None) == tl.TL_EUNSUPPORTED
+    # fused decode: M <= 16; M = 1 up to K = 8192; M >= 2 while M (rounded up) * K <= 72 K, on
+    # the multi-token kernel's K values
+    fused = lib.tl_linear_decode_fused
+    assert fused(ok, ok, ok, ok, None, 17, 128, 1024, ok, tl.TL_F32, None, None, None, None) == tl.TL_EUNSUPPORTED
+    assert fused(ok, ok, ok, ok, None, 1, 128, 9216, ok, tl.TL_F32, None, None, None, None) == tl.TL_EUNSUPPORTED
+    assert fused(ok, ok, ok, ok, None, 16, 128, 5120, ok, tl.TL_F32, None, None, None, None) == tl.TL_EUNSUPPORTED
+    assert fused(ok, ok, ok, ok, None, 2, 128, 6144, ok, tl.TL_F32, None, None, None, None) == tl.TL_EUNSUPPORTED
+    assert fused(ok, ok, ok, ok, None, 5, 128, 17408, ok, tl.TL_F32, None, None, None, None) == tl.TL_EUNSUPPORTED
     # negative sizes, NULLs, misalignment, dtypes
     assert lib.tl_linear_prefill(ok, ok, ok, ok, ok, -1, 128, 1024, ok, tl.TL_F32, None, None, 0, None) == tl.TL_EINVAL
     assert lib.tl_linear_prefill(ok, ok, ok, None, ok, 4, 128, 1024, ok, tl.TL_F32, None, None, 0, None) == tl.TL_EINVAL

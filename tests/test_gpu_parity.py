@@ -231,6 +231,33 @@ def test_decode_fused_clusters_of_four(tl, K):
     _compare(L, acc1.cpu().numpy(), y1, 4)
 
 
+@pytest.mark.parametrize("M,K,N,signed", [(2, 1024, 256, False), (3, 5120, 256, True), (4, 17408, 256, False),
+                                           (5, 8192, 384, False), (8, 5120, 256, True),
+                                           (9, 4096, 256, False), (16, 2048, 384, True), (16, 4096, 256, False)])
+def test_decode_fused_multi_token(tl, M, K, N, signed):
+    """2 <= M <= 16 tokens (M K <= 72 K) in one launch equal the two-kernel path bit for bit,
+    including the quantised tokens and their scales."""
+    L = synth.config_inputs("decode", M=M, N=N, K=K)
+    packed, qT, sw = pack_dev(tl, L)
+    x = x_dev(L)
+    signs = None
+    if signed:
+        signs = dev(np.where(np.random.default_rng(K + M).random(K) < 0.5, -1, 1).astype(np.int8))
+    acc2 = torch.empty((M, L.N), dtype=torch.int32, device="cuda")
+    xq, sx = tl.tl_rotate_quant_act(x, signs=signs, xq_dtype=tl.TL_I8)
+    y2 = tl.tl_linear_decode(packed, qT, sw, xq, sx, L.N, L.K, 4, acc_dbg=acc2)
+    acc1 = torch.full((M, L.N), ACC_SENTINEL, dtype=torch.int32, device="cuda")
+    xq1 = torch.zeros((M, K), dtype=torch.int8, device="cuda")
+    sx1 = torch.zeros((M,), dtype=torch.float32, device="cuda")
+    y1 = tl.tl_linear_decode_fused(packed, qT, sw, x, L.N, L.K, 4, signs=signs, acc_dbg=acc1,
+                                   xq_out=xq1, sx_out=sx1)
+    check_status(tl)
+    assert torch.equal(xq1, xq) and torch.equal(sx1, sx)
+    assert torch.equal(acc1, acc2) and torch.equal(y1, y2)
+    if not signed:
+        _compare(L, acc1.cpu().numpy(), y1, 4, frobenius=False)
+
+
 def test_decode_fused_full_size(tl):
     L = synth.config_inputs("decode")
     packed, qT, sw = pack_dev(tl, L)
