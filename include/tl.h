@@ -39,7 +39,8 @@ extern "C" {
 enum tl_status {
   TL_OK = 0,
   TL_EINVAL = 1,        /* NULL pointer, negative size, misaligned pointer, bad dtype */
-  TL_EUNSUPPORTED = 2,  /* K not a multiple of 1024 or > 32768, N % 128, M > 32 on decode */
+  TL_EUNSUPPORTED = 2,  /* a shape outside the entry point's range (K % 1024, K > 32768,
+                           N % 128, M > 32 on decode; the others' limits are stated with them) */
   TL_ECUDA = 3,         /* a CUDA runtime call or kernel launch failed */
   TL_ETIMEOUT = 4,      /* a bounded device-side wait gave up (via tl_get_status) */
   TL_EDATA = 5,         /* input data out of range, e.g. a code not in {-1,0,1} (via tl_get_status) */
@@ -248,7 +249,9 @@ int tl_linear_decode_f32act(const uint8_t* packed, const uint16_t* s, const floa
  *   scale  out fp32 [R, H/128]
  * Per 128-element group: a = max |x|; inv = fl32(127/a);
  * q = clamp(rne(fl32(x inv)), -127, 127); scale = fl32(a/127); a = 0 gives
- * q = 0 and scale = 0.
+ * q = 0 and scale = 0. A NaN product codes to 0 (what an fp32 -> int
+ * conversion gives it); a group whose maximum is below 127/FLT_MAX makes inv
+ * +inf, so its non-zero elements code to +-127 and its zeros to 0.
  *
  * tl_codec_dequant_add decompresses the peers' parts and adds them to the own:
  *   own          in  bf16 [R, H], the rank's own part (not compressed)
