@@ -5,7 +5,13 @@
 // is the idea of §5 "効かなかったもの" (a dp4a decode GEMV), here computing
 // exactly the quantised layer so that decode and prefill agree bit for bit.
 //
-// Each CTA owns 32 consecutive output rows, 4 per warp. Its first weight
+// Kernels here: decode1_kernel (M = 1), decodem_kernel (2 <= M <= 16 while
+// M * K <= 72 K), decode_kernel (the remaining M <= 32, K in shared-memory
+// slabs) and decode1f_kernel (M = 1 with the rotation inside, in clusters);
+// decode_fused_m.cu holds the fused multi-token kernel.
+//
+// Each CTA owns 32 consecutive output rows, 4 per warp (16 and 2 above
+// K = 8192, where a row fills the register ring). Its first weight
 // loads are issued at entry, before the kernel waits (programmatic dependent
 // launch) for the activations of the preceding kernel, so the 2-bit weight
 // stream of one layer overlaps the tail of the previous one. The packed
