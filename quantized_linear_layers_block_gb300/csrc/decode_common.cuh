@@ -51,7 +51,10 @@ struct MTTraits {
   // M = 8: 20.8 -> 19.4 us at K = 5120; at MT = 2 the 4-row version measured 10.1 against 7.2 us)
   static constexpr int GR = MT >= 16 ? 1 : ((MT >= 4 && RPW == 4) ? 4 : 2);
   static constexpr int NG = RPW / GR;                            // row groups per warp
-  static constexpr int RC = PL * NG < 3 ? PL * NG : 3;           // (group, chunk) steps in flight
+  // (group, chunk) steps in flight: 8 above K = 8192, as the M = 1 kernel there
+  // (M = 4 at K = 17408: 19.2 -> 18.1 us), 3 below
+  static constexpr int RC0 = PL > 8 ? 8 : 3;
+  static constexpr int RC = PL * NG < RC0 ? PL * NG : RC0;
   static constexpr int QSTRIDE = ROWS + 4;
   static constexpr int LOG2MT = MT == 2 ? 1 : (MT == 4 ? 2 : (MT == 8 ? 3 : 4));
   static constexpr size_t SMEM = static_cast<size_t>(MT) * (PL * kBlock / 32) * 36;
