@@ -25,6 +25,19 @@
  *   - Return value: a tl_status code. Errors found on the device (bounded waits
  *     that gave up, codes outside {-1,0,1}) are recorded in a per-device status
  *     word and reported by tl_get_status.
+ *   - Weights before activations: the GEMM kernels (tl_linear_prefill,
+ *     tl_linear_prefill_noalloc, tl_linear_decode, tl_linear_decode_fused,
+ *     tl_linear_decode_f32act) start loading the weight arrays (packed, qT, sw,
+ *     s) BEFORE they wait for the preceding kernel in the stream (programmatic
+ *     dependent launch), so that the weight stream overlaps that kernel. The
+ *     weights must therefore be complete before the preceding kernel in the
+ *     stream begins: they must not be written by the kernel launched
+ *     immediately before the call. tl_pack_weights meets this by itself (it
+ *     ends with a launch that starts only after its outputs are complete), so
+ *     its outputs may be used by the very next call; weights written by other
+ *     code need any other operation (a kernel, a copy, an event wait) between
+ *     the writer and the call. The activations (x, xq, xr, sx) and every output
+ *     are touched only after the wait, so they may come from the preceding kernel.
  */
 #ifndef TL_H_
 #define TL_H_
@@ -61,11 +74,15 @@ const char* tl_strerror(int status);
 int tl_version(void);
 
 /*
- * Bytes of the three packed-weight arrays for an N x K layer:
+ * Bytes of the three packed-weight arrays for an N x K layer (Qiita item
+ * ecc183fae033565af7cb, 前提: the {-1,0,+1} codes in a 2-bit representation
+ * with one fp16 scale per 128 elements; §4 "効いた高速化": the scales as an
+ * int8 ratio q per group times a per-row maximum):
  *   packed  N * K / 4  (uint8; 2 bits per code)
  *   qT      (K/128) * N (int8; q transposed, group-major)
- *   sw      N * 4       (fp32)
- * Any output pointer may be NULL. Errors: TL_EINVAL, TL_EUNSUPPORTED.
+ *   sw      N * 4       (fp32; smax / 127 per row)
+ * Any output pointer may be NULL. N < 0 or K <= 0 returns TL_EINVAL; K not a
+ * multiple of 1024, K > 32768 or N not a multiple of 128 returns TL_EUNSUPPORTED.
  */
 int tl_packed_sizes(int N, int K, size_t* packed_bytes, size_t* qT_bytes, size_t* sw_bytes);
 
@@ -99,7 +116,10 @@ int tl_pack_weights(const int8_t* codes, const uint16_t* s, int N, int K,
  *   sx        out fp32 [M]
  * Per token: xr = fl32 butterflies with strides 1,2,...,512 then x 1/32;
  * a = max |xr|; inv = fl32(127/a); xq = clamp(rne(fl32(xr inv)), +-127);
- * sx = fl32(a/127); a token with a = 0 gives xq = 0 and sx = 0.
+ * sx = fl32(a/127); a token with a = 0 gives xq = 0 and sx = 0. A token
+ * with 0 < a < 127/FLT_MAX (bf16 subnormals only) makes inv = +inf: its
+ * non-zero elements code to +-127 and its exact zeros to 0 (the fp32 -> int
+ * conversion of the NaN 0 * inf), with sx = fl32(a/127) (possibly 0).
  */
 int tl_rotate_quant_act(const uint16_t* x, int M, int K, const int8_t* signs,
                         void* xq, int xq_dtype, float* sx, void* stream);
@@ -109,8 +129,10 @@ int tl_rotate_quant_act(const uint16_t* x, int M, int K, const int8_t* signs,
  * CTAs: the output tiles that do not fill a whole round of SMs (all of them
  * when there are fewer tiles than SMs) are cut into equal ranges of
  * 1024-column chunks, one per CTA, and a cut tile's partial int32 sums meet in
- * a 64 KB slot of the workspace (plus 4 bytes per slot). With a smaller (or
- * NULL) workspace the call still succeeds, unsplit.
+ * a slot of the workspace (512 bytes per token of the tile: 64 KB for a
+ * 128-token tile, 8 KB for the 16-token tiles of a batch of at most 16
+ * tokens; plus 4 bytes per slot). With a smaller (or NULL) workspace the call
+ * still succeeds, unsplit.
  */
 int tl_prefill_workspace_size(int M, int N, int K, size_t* bytes);
 
@@ -125,7 +147,15 @@ int tl_prefill_workspace_size(int M, int N, int K, size_t* bytes);
  *   y                out [M, N], y_dtype TL_BF16 (rne of the fp32 value) or TL_F32
  *   acc_dbg          optional out int32 [M, N]: the exact integer accumulator
  *   workspace        optional device scratch of ws_bytes (see
- *                    tl_prefill_workspace_size); the call clears what it uses
+ *                    tl_prefill_workspace_size). It must hold zeros before its
+ *                    first use (zero it once after allocating it); every call
+ *                    that completes leaves it all zero again, so it needs no
+ *                    clearing between calls. After a call whose kernel gave up
+ *                    (TL_ETIMEOUT from tl_get_status) zero it again. Calls that
+ *                    can overlap on the GPU must not share a workspace.
+ * Batches of at most 16, 32 or 64 tokens run on tiles of that many tokens (the
+ * MMA's N), so that the weights are expanded once for the batch without
+ * tensor-core work on padding; larger batches run on 128-token tiles.
  * The integer accumulator is exact: the tensor cores take the int8 values as
  * fp16 (exact), sum each 1024-column block in fp32 (every partial sum is an
  * integer below 127*127*1024 < 2^24, hence exact) and the blocks are added in
@@ -137,12 +167,17 @@ int tl_linear_prefill(const uint8_t* packed, const int8_t* qT, const float* sw,
                       void* workspace, size_t ws_bytes, void* stream);
 
 /*
- * Decode (1 <= M <= 32) ternary linear layer on the CUDA cores: streams the
- * 2-bit weights once, decodes them in registers and takes int8 dot products
- * (dp4a); same acc and y as tl_linear_prefill, bit for bit.
+ * Decode (1 <= M <= 32) ternary linear layer on the CUDA cores (Qiita item
+ * ecc183fae033565af7cb §4 "効いた高速化" defines the quantised layer it
+ * computes; §5 "効かなかったもの" the int8-activation dp4a decode GEMV it is
+ * built on): streams the 2-bit weights once, decodes them in registers and
+ * takes int8 dot products (dp4a); same acc and y as tl_linear_prefill, bit
+ * for bit.
  *
  *   xq   int8 [M, K] (tl_rotate_quant_act with TL_I8); other arguments as
  *        for tl_linear_prefill. M > 32 returns TL_EUNSUPPORTED.
+ * The weights are read before the wait on the preceding kernel (see the
+ * conventions above).
  */
 int tl_linear_decode(const uint8_t* packed, const int8_t* qT, const float* sw,
                      const int8_t* xq, const float* sx, int M, int N, int K,
@@ -189,7 +224,8 @@ int tl_linear_decode_fused(const uint8_t* packed, const int8_t* qT, const float*
  * Arguments, layout, result and errors are those of tl_linear_prefill. When
  * the problem has fewer output tiles than SMs, K is split and the partial
  * int32 sums meet in a static device array of TL_NOALLOC_SCRATCH_BYTES owned
- * by the library; the call clears the part it uses before the kernel. If that
+ * by the library; the call clears the part it uses before the kernel (so a
+ * call that gave up earlier leaves nothing behind for the next). If that
  * part would exceed the array (see tl_prefill_workspace_size) the call returns
  * TL_ENOSPACE and launches nothing. With at least as many tiles as SMs only
  * the last partial round is split; if that does not fit either, every tile
@@ -198,8 +234,13 @@ int tl_linear_decode_fused(const uint8_t* packed, const int8_t* qT, const float*
  *
  * - Every call shares the one array per device: calls that can overlap on the
  *   GPU (other streams, other host threads) race on it; serialise them.
- * - The first call on a device looks up the array's device address; make that
- *   first call before any stream capture.
+ * - The first call on a device looks up the array's device address, and the
+ *   first prefill call of either entry point on a device loads the library's
+ *   kernels together with the array, which reserves its 8 MiB of device memory
+ *   and may synchronise the device. Make one call during set-up, before any
+ *   stream capture and before the device memory is handed out.
+ * - The library caches that address (and its status word's) per device: do not
+ *   keep using it after cudaDeviceReset.
  */
 int tl_linear_prefill_noalloc(const uint8_t* packed, const int8_t* qT, const float* sw,
                               const uint16_t* xq, const float* sx, int M, int N, int K,

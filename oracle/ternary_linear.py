@@ -27,7 +27,9 @@ Readings where the pages are silent (each one is listed in the design notes):
     sw[n] = fl32(smax / 127); a zero row gives q = 0 and sw = 0.
   * Activation quantisation is symmetric over the whole token:
     a = max_k |xr|; inv = fl32(127 / a); xq = clamp(rne(fl32(xr inv)), -127, 127);
-    sx = fl32(a / 127); a token with a = 0 gives xq = 0, sx = 0.
+    sx = fl32(a / 127); a token with a = 0 gives xq = 0, sx = 0. A token with
+    0 < a < 127/FLT_MAX (bf16 subnormals) overflows inv to +inf: its non-zero
+    elements code to +-127 and its exact zeros (0 * inf = NaN) to 0.
   * The rotated activations stay fp32 (no bf16 rounding before quantisation).
   * Epilogue: y = fl32(fl32(fl32(acc) sw[n]) sx[m]); optional rne to bf16.
   * The 2-bit packed layout is this library's own format (the pages only say
@@ -135,10 +137,19 @@ def quantize_per_token(xr: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
         a = np.max(np.abs(xr[m]))
         if a == 0:
             continue
-        inv = np.float32(QMAX) / a
-        t = xr[m] * inv
+        # a below 127 / FLT_MAX (about 3.7e-37; a token of bf16 subnormals)
+        # makes the fp32 quotient overflow to +inf
+        with np.errstate(over="ignore"):
+            inv = np.float32(np.float32(QMAX) / a)
+        with np.errstate(over="ignore", invalid="ignore"):
+            t = (xr[m] * inv).astype(np.float32)
+        # Reading for that case: a non-zero element times +inf is +-inf and
+        # clamps to +-127; an exact zero times +inf is NaN and codes to 0, the
+        # value an fp32 -> int conversion gives a NaN. Finite products are
+        # rounded half to even and clamped as usual.
+        t = np.where(np.isnan(t), np.float32(0), t)
         xq[m] = np.clip(np.rint(t), -QMAX, QMAX).astype(np.int8)
-        sx[m] = a / np.float32(QMAX)
+        sx[m] = np.float32(a / np.float32(QMAX))
     return xq, sx
 
 

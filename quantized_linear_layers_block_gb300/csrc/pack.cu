@@ -65,12 +65,22 @@ pack_kernel(const int8_t* __restrict__ codes, const uint16_t* __restrict__ s, in
   if (bad) set_status(status, TL_EDATA);
 }
 
+// Launched without programmatic serialization right after the pack kernel, so
+// it starts only once the packed weights are complete and visible. The
+// library's GEMM kernels read weights before they wait on the preceding kernel
+// in the stream; with this launch in between, that preceding kernel is not
+// the one that wrote the weights.
+__global__ void pack_done_kernel() {}
+
 }  // namespace
 
 cudaError_t launch_pack(const int8_t* codes, const uint16_t* s, int N, int K, uint32_t* packed,
                         int8_t* qT, float* sw, int* status, cudaStream_t st) {
   const int blocks = (N + kPackWarps - 1) / kPackWarps;
   pack_kernel<<<blocks, kPackWarps * 32, 0, st>>>(codes, s, N, K, packed, qT, sw, status);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  pack_done_kernel<<<1, 32, 0, st>>>();
   return cudaGetLastError();
 }
 

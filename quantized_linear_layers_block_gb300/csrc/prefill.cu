@@ -14,10 +14,14 @@
 // equals the int8 GEMM's bit for bit.
 //
 // Work: persistent CTAs (one per SM) over output tiles of 128 weight rows x
-// 128 tokens; the MMA computes D[n, m] = sum_k W[n, k] X[m, k] (y transposed,
+// BN tokens; the MMA computes D[n, m] = sum_k W[n, k] X[m, k] (y transposed,
 // weight rows on the tensor-memory lanes), 256 columns of K per pipeline
-// stage (16 MMAs of K = 16).
-// Roles of the 20 warps:
+// stage (16 MMAs of K = 16). BN is 128 for long batches and 64, 32 or 16
+// (the MMA's N) when the batch has at most that many tokens: a weight tile is
+// then expanded once for the whole batch while the tensor cores do no work on
+// padding tokens, and the smaller activation tiles leave shared memory to a
+// deeper weight ring, which the weight stream needs at these sizes.
+// Roles of the warps (20 with two expansion warps per lane quarter, 28 with four):
 //   warp 0       weight producer: packed 2-bit codes of the 128 rows and their
 //                two q bytes per row and stage into a 4-deep ring (TMA); it
 //                starts before the kernel waits for the preceding one
@@ -30,20 +34,22 @@
 //                the activations land), issues the stage's 16 MMAs and commits
 //                the A slot and the activation slot free: any other instruction
 //                in that thread costs tensor-pipe time, so it does nothing else.
-//   warps 4-11   expansion, two warps per 32-lane quarter of tensor memory: lane
-//                = weight row; warp `part` (0 or 1) turns the 128 codes of q
-//                group `part` of the stage into 64 fp16 pairs in registers and
-//                stores them into tensor memory as the MMA's A operand
+//   expansion    EPQ (2 or 4) warps per 32-lane quarter of tensor memory: lane
+//                = weight row; warp `part` turns its 256 / EPQ codes of the
+//                stage (q group part / (EPQ / 2)) into fp16 pairs in registers
+//                and stores them into tensor memory as the MMA's A operand
 //                (tcgen05.st), then waits for the stage's activations and
 //                arrives on the A slot's full barrier.
-//   warps 12-19  drain + epilogue, two per quarter (64 tokens each): after each
+//   drain        two warps per quarter (BN / 2 tokens each): after each
 //                1024-column chunk add the fp32 accumulator (double buffered)
 //                into int32 totals in registers; at the end of a tile write
 //                y = (fl32(acc) sw[n]) sx[m].
-// Tensor memory (512 columns x 128 lanes): 2 A slots of 128 columns at [0,256),
-// fp32 accumulators at [256,384) and [384,512).
+// Tensor memory (512 columns x 128 lanes): NA A slots of 128 columns from
+// column 0, then two fp32 accumulators of BN columns.
 // When the problem has fewer tiles than SMs, K is split across CTAs; partial
-// int32 sums meet in a caller workspace and the last CTA of a tile finishes it.
+// int32 sums meet in a caller workspace and the last CTA of a tile finishes it
+// and returns the tile's part of the workspace to zero, so the workspace needs
+// zeroing only once, when it is allocated.
 #include "tl_internal.cuh"
 
 #include <cuda_bf16.h>
@@ -56,45 +62,54 @@ namespace tl {
 namespace {
 
 constexpr int BM = 128;             // weight rows per tile (MMA M, TMEM lanes)
-constexpr int BN = 128;             // tokens per tile (MMA N)
 constexpr int BK = 256;             // columns of K per pipeline stage (two q groups)
 constexpr int BOX_K = 64;           // columns per 128-byte swizzled activation box
-constexpr int NW = 4;               // weight ring depth
-constexpr int NB = 3;               // activation ring depth
-constexpr int NA = 2;               // tensor-memory A slots
 constexpr int STAGES_PER_CHUNK = kBlock / BK;
 constexpr int UMMA_K = 16;
 constexpr int MMAS_PER_STAGE = BK / UMMA_K;
-
-constexpr int BOX_BYTES = BN * BOX_K * 2;     // 16 KB
-constexpr int B_BYTES = BN * BK * 2;          // 64 KB fp16 activation tile (four boxes)
 constexpr int P_BYTES = BM * (BK / 4);        // 8 KB packed codes
 constexpr int Q_BYTES = BM * (BK / kGroup);   // 256 q bytes: [2 groups][128 rows]
 constexpr uint32_t W_TX = P_BYTES + Q_BYTES;
-
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t A_COLS = BK / 2;           // 128 columns of fp16 pairs per A slot
-constexpr uint32_t A_COL0 = 0;                // A slot a at columns 128 a
-constexpr uint32_t D_COL0 = 256;              // accumulators at 256 and 384
+constexpr int WARP_WLOAD = 0, WARP_MMA = 1, WARP_BLOAD = 2, WARP_EXP0 = 4;
+constexpr int N_DRAIN_WARPS = 8;
 
-constexpr int WARP_WLOAD = 0, WARP_MMA = 1, WARP_BLOAD = 2, WARP_EXP0 = 4, WARP_DRAIN0 = 12;
-constexpr int N_EXP_WARPS = 8, N_DRAIN_WARPS = 8;
-constexpr int kThreads = (WARP_DRAIN0 + N_DRAIN_WARPS) * 32;
-
-constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
-
-struct Smem {
+// Per tile width BN (tokens): ring depths (NW weight stages, NB activation
+// stages, NA tensor-memory A slots) and expansion warps per lane quarter (EPQ).
+template <int BN_, int NW_, int NB_, int NA_, int EPQ_>
+struct Cfg {
+  static constexpr int BN = BN_, NW = NW_, NB = NB_, NA = NA_, EPQ = EPQ_;
+  static constexpr int BOX_BYTES = BN * BOX_K * 2;   // one 128-byte swizzled box
+  static constexpr int B_BYTES = BN * BK * 2;        // fp16 activation tile of a stage (four boxes)
+  static constexpr int N_EXP_WARPS = 4 * EPQ;
+  static constexpr int WARP_DRAIN0 = WARP_EXP0 + N_EXP_WARPS;
+  static constexpr int kThreads = (WARP_DRAIN0 + N_DRAIN_WARPS) * 32;
+  static constexpr int EXP_COLS = A_COLS / EPQ;      // tensor-memory columns per expansion warp
+  static constexpr int EXP_WORDS = EXP_COLS / 8;     // packed 16-code words per lane and stage
+  static constexpr uint32_t D_COL0 = NA * A_COLS;    // accumulators at D_COL0 + {0, BN}
+  static constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
   // byte offsets inside the 1024-aligned dynamic shared memory block
-  static constexpr int b = 0;
-  static constexpr int p = b + NB * B_BYTES;
-  static constexpr int q = p + NW * P_BYTES;
-  static constexpr int bar = q + NW * Q_BYTES;
+  static constexpr int sb = 0;
+  static constexpr int sp = sb + NB * B_BYTES;
+  static constexpr int sq = sp + NW * P_BYTES;
+  static constexpr int sbar = sq + NW * Q_BYTES;
   // wfull[NW] wempty[NW] bfull[NB] bempty[NB] afull[NA] aempty[NA] dfull[2] dempty[2] fin rdv1 rdv2
   static constexpr int n_bars = 2 * NW + 2 * NB + 2 * NA + 2 + 2 + 3;
-  static constexpr int misc = bar + n_bars * 8;
-  static constexpr int total = misc + 16;
+  static constexpr int smisc = sbar + n_bars * 8;
+  static constexpr int stotal = smisc + 16;
+  static_assert(stotal + 1024 <= 232448, "shared memory budget");
+  static_assert(D_COL0 + 2 * BN <= TMEM_COLS, "tensor memory budget");
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
+  static_assert(EPQ == 2 || EPQ == 4, "expansion split");
 };
-static_assert(Smem::total + 1024 <= 232448, "shared memory budget");
+// 128 tokens: the activation ring fills shared memory; 64, 32 and 16 tokens:
+// deeper weight rings and a third A slot; four expansion warps per quarter
+// where the drain's totals are few enough for the smaller register budget.
+using Cfg128 = Cfg<128, 4, 3, 2, 2>;
+using Cfg64 = Cfg<64, 8, 4, 3, 2>;
+using Cfg32 = Cfg<32, 12, 4, 3, 4>;
+using Cfg16 = Cfg<16, 16, 4, 3, 4>;
 
 // Work schedule. Tiles [0, full) are whole units, dealt round-robin to the
 // grid (full is a multiple of the grid, so every CTA gets the same number).
@@ -195,17 +210,52 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&v)
       : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Adds the fp32 accumulator columns [col, col + W) of this warp's lanes,
+// integers below 2^24 in magnitude, to the int32 totals.
+template <int W>
+__device__ __forceinline__ void drain_add(uint32_t taddr, int (&tot)[W]) {
+  if constexpr (W == 8) {
+    uint32_t v[8];
+    tmem_ld_32x32b_x8(taddr, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) tot[i] += __float2int_rn(__uint_as_float(v[i]));
+  } else {
+#pragma unroll
+    for (int p = 0; p < W / 16; ++p) {
+      uint32_t v[16];
+      tmem_ld_32x32b_x16(taddr + p * 16, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) tot[p * 16 + i] += __float2int_rn(__uint_as_float(v[i]));
+    }
+  }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_p,
                const __grid_constant__ CUtensorMap map_q, const float* __restrict__ sw,
                const float* __restrict__ sx, int M, int N, Work work, void* __restrict__ y,
                int y_dtype, int32_t* __restrict__ acc_dbg, int32_t* __restrict__ ws_acc,
                int* __restrict__ ws_cnt, int* status) {
+  constexpr int BN = C::BN, NW = C::NW, NB = C::NB, NA = C::NA;
+  constexpr int N_EXP_WARPS = C::N_EXP_WARPS, WARP_DRAIN0 = C::WARP_DRAIN0;
+  constexpr int HB = BN / 2;                 // tokens per drain warp
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar0 = sbase + Smem::bar;
+  const uint32_t bar0 = sbase + C::sbar;
   auto wfull = [&](int i) { return bar0 + 8u * i; };
   auto wempty = [&](int i) { return bar0 + 8u * (NW + i); };
   auto bfull = [&](int i) { return bar0 + 8u * (2 * NW + i); };
@@ -217,9 +267,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
   const uint32_t fin = bar0 + 8u * (2 * NW + 2 * NB + 2 * NA + 4);
   const uint32_t rdv1 = fin + 8u;
   const uint32_t rdv2 = fin + 16u;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Smem::misc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem::misc + 4);
-  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + Smem::misc + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::smisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::smisc + 4);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::smisc + 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -234,8 +284,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
       mbar_init(bempty(i), 1);
     }
     for (int i = 0; i < NA; ++i) {
-      // a stage is ready for the MMAs when all 8 expansion warps have written
-      // their half of its A slot and have seen its activation tile land
+      // a stage is ready for the MMAs when all expansion warps have written
+      // their part of its A slot and have seen its activation tile land
       mbar_init(afull(i), N_EXP_WARPS);
       mbar_init(aempty(i), 1);
     }
@@ -285,8 +335,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
             }
             const int k0 = c * kBlock + st * BK;
             mbar_arrive_expect_tx(wfull(w), W_TX);
-            tma_load_2d(sbase + Smem::p + w * P_BYTES, &map_p, k0 / 4, nt * BM, wfull(w));
-            tma_load_2d(sbase + Smem::q + w * Q_BYTES, &map_q, nt * BM, k0 / kGroup, wfull(w));
+            tma_load_2d(sbase + C::sp + w * P_BYTES, &map_p, k0 / 4, nt * BM, wfull(w));
+            tma_load_2d(sbase + C::sq + w * Q_BYTES, &map_q, nt * BM, k0 / kGroup, wfull(w));
           }
         }
       }
@@ -317,11 +367,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
               break;
             }
             const int k0 = c * kBlock + st * BK;
-            mbar_arrive_expect_tx(bfull(b), B_BYTES);
+            mbar_arrive_expect_tx(bfull(b), C::B_BYTES);
 #pragma unroll
             for (int bx = 0; bx < BK / BOX_K; ++bx)
-              tma_load_2d(sbase + Smem::b + b * B_BYTES + bx * BOX_BYTES, &map_x, k0 + bx * BOX_K,
-                          mt * BN, bfull(b));
+              tma_load_2d(sbase + C::sb + b * C::B_BYTES + bx * C::BOX_BYTES, &map_x,
+                          k0 + bx * BOX_K, mt * BN, bfull(b));
           }
         }
       }
@@ -336,8 +386,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
       uint32_t it = 0, cc = 0;
       bool ok = true;
       // descriptor of activation slot 0, first box, first 16 columns: boxes are
-      // 16 KB apart, slots 64 KB apart, and each 16-column step is 32 bytes
-      const uint64_t desc0 = smem_desc_sw128(sbase + Smem::b);
+      // BOX_BYTES apart, slots B_BYTES apart, and each 16-column step is 32 bytes
+      const uint64_t desc0 = smem_desc_sw128(sbase + C::sb);
       const int npieces = num_pieces(work, blockIdx.x);
       for (int k = 0; ok && k < npieces; ++k) {
         const Piece pc = get_piece(work, blockIdx.x, k);
@@ -351,7 +401,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
             break;
           }
           tc_fence_after();
-          const uint32_t d_addr = tmem + D_COL0 + buf * BN;
+          const uint32_t d_addr = tmem + C::D_COL0 + buf * BN;
           for (int st = 0; st < STAGES_PER_CHUNK; ++st, ++it) {
             const int b = it % NB;
             const int a = it % NA;
@@ -364,12 +414,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
               break;
             }
             tc_fence_after();
-            const uint64_t dslot = desc0 + static_cast<uint64_t>((b * B_BYTES) >> 4);
-            const uint32_t aslot = tmem + A_COL0 + A_COLS * a;
+            const uint64_t dslot = desc0 + static_cast<uint64_t>((b * C::B_BYTES) >> 4);
+            const uint32_t aslot = tmem + A_COLS * a;
 #pragma unroll
             for (int j = 0; j < MMAS_PER_STAGE; ++j) {
-              const uint32_t boff = (j >> 2) * (BOX_BYTES >> 4) + (j & 3) * (32 >> 4);
-              mma_f16_ts(d_addr, aslot + 8u * j, dslot + boff, IDESC, (st | j) != 0);
+              const uint32_t boff = (j >> 2) * (C::BOX_BYTES >> 4) + (j & 3) * (32 >> 4);
+              mma_f16_ts(d_addr, aslot + 8u * j, dslot + boff, C::IDESC, (st | j) != 0);
             }
             tc_commit(aempty(a));
             tc_commit(bempty(b));
@@ -382,10 +432,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
       mbar_wait(fin, 0, nullptr);
     }
   } else if (warp >= WARP_EXP0 && warp < WARP_EXP0 + N_EXP_WARPS) {
-    // two warps per lane quarter; warp `part` expands columns [128 part, 128 part + 128)
-    // of every stage, i.e. q group `part` of the stage
+    // EPQ warps per lane quarter; warp `part` expands tensor-memory columns
+    // [EXP_COLS part, EXP_COLS (part + 1)) of every stage's A slot: the codes
+    // 16 EXP_WORDS part .. of its row in the stage, all of one q group
     const int quarter = warp & 3;
     const int part = (warp - WARP_EXP0) >> 2;
+    const int grp = part / (C::EPQ / 2);
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     uint32_t it = 0;
@@ -408,10 +460,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
             ok = false;
             break;
           }
-          const uint4* prow =
-              reinterpret_cast<const uint4*>(smem + Smem::p + w * P_BYTES + row * (BK / 4) + part * 32);
-          const uint4 pk0 = prow[0], pk1 = prow[1];
-          const int qv = static_cast<int8_t>(smem[Smem::q + w * Q_BYTES + part * BM + row]);
+          const uint4* prow = reinterpret_cast<const uint4*>(smem + C::sp + w * P_BYTES +
+                                                             row * (BK / 4) + part * (C::EXP_WORDS * 4));
+          uint4 pk[C::EXP_WORDS / 4];
+#pragma unroll
+          for (int i = 0; i < C::EXP_WORDS / 4; ++i) pk[i] = prow[i];
+          const int qv = static_cast<int8_t>(smem[C::sq + w * Q_BYTES + grp * BM + row]);
           // the slot is refilled by TMA (async proxy): order these ordinary
           // loads before the release, or the copy can overtake them
           fence_proxy_async_smem();
@@ -420,10 +474,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
           const __half qh = __int2half_rn(qv);
           const __half2 q2 = __halves2half2(qh, qh);
           uint32_t out[32];
-          expand_word(pk0.x, q2, out + 0);
-          expand_word(pk0.y, q2, out + 8);
-          expand_word(pk0.z, q2, out + 16);
-          expand_word(pk0.w, q2, out + 24);
+          expand_word(pk[0].x, q2, out + 0);
+          expand_word(pk[0].y, q2, out + 8);
+          expand_word(pk[0].z, q2, out + 16);
+          expand_word(pk[0].w, q2, out + 24);
           // the A slot is free once the MMAs of the stage that used it last completed
           const bool free_slot = mbar_wait(aempty(a), aph ^ 1u, abort_flag);
           if (!__all_sync(0xffffffffu, free_slot)) {
@@ -432,13 +486,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
             break;
           }
           tc_fence_after();
-          const uint32_t aslot = lane_base + A_COL0 + A_COLS * a + 64u * part;
+          const uint32_t aslot = lane_base + A_COLS * a + C::EXP_COLS * part;
           tmem_st_32x32b_x32(aslot, out);
-          expand_word(pk1.x, q2, out + 0);
-          expand_word(pk1.y, q2, out + 8);
-          expand_word(pk1.z, q2, out + 16);
-          expand_word(pk1.w, q2, out + 24);
-          tmem_st_32x32b_x32(aslot + 32, out);
+          if constexpr (C::EXP_WORDS == 8) {
+            expand_word(pk[1].x, q2, out + 0);
+            expand_word(pk[1].y, q2, out + 8);
+            expand_word(pk[1].z, q2, out + 16);
+            expand_word(pk[1].w, q2, out + 24);
+            tmem_st_32x32b_x32(aslot + 32, out);
+          }
           tmem_wait_st();
           tc_fence_before();
           const bool landed = mbar_wait(bfull(b), bph, abort_flag);
@@ -464,9 +520,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
       const Piece pc = get_piece(work, blockIdx.x, k);
       const int nt = pc.nt, mt = pc.mt, c0 = pc.c0, c1 = pc.c1;
       const int slot = pc.slot;
-      int tot[64];
+      int tot[HB];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) tot[j] = 0;
+      for (int j = 0; j < HB; ++j) tot[j] = 0;
       for (int c = c0; c < c1; ++c, ++cc) {
         const uint32_t buf = cc & 1u;
         const uint32_t dph = (cc >> 1) & 1u;
@@ -477,32 +533,26 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
           break;
         }
         tc_fence_after();
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          uint32_t v[16];
-          tmem_ld_32x32b_x16(lane_base + D_COL0 + buf * BN + half * 64 + p * 16, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) tot[p * 16 + i] += __float2int_rn(__uint_as_float(v[i]));
-        }
+        drain_add<HB>(lane_base + C::D_COL0 + buf * BN + half * HB, tot);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(dempty(buf));
       }
       const int n = nt * BM + row;
-      const int mbase = mt * BN + half * 64;
+      const int mbase = mt * BN + half * HB;
       bool finish = ok;
       if (slot >= 0) {
         // Rendezvous of the drain warps through two mbarriers (bounded waits):
         // every warp adds its partial sums into the tile's workspace slot
         // ([token][row] within the tile), the leader counts the tile's finished
-        // splits, and the CTA that completes the tile writes it.
-        int32_t* wsl = ws_acc + static_cast<size_t>(slot) * (BM * BN) + (half * 64) * BM + row;
+        // splits, and the CTA that completes the tile writes it and returns the
+        // slot and its count to zero for the next call.
+        int32_t* wsl = ws_acc + static_cast<size_t>(slot) * (BM * BN) + (half * HB) * BM + row;
         const uint32_t rp = ku & 1u;
         ++ku;
         if (ok) {
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
+          for (int j = 0; j < HB; ++j) {
             const int m = mbase + j;
             if (m < M) atomicAdd(wsl + j * BM, tot[j]);
           }
@@ -516,6 +566,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
             if (!*abort_flag) {
               __threadfence();
               last = atomicAdd(ws_cnt + slot, 1) == pc.contrib - 1;
+              // every contributor has counted itself: nothing reads the count again
+              if (last) ws_cnt[slot] = 0;
             }
           } else {
             fail();
@@ -532,16 +584,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
         if (finish) {
           __threadfence();
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
+          for (int j = 0; j < HB; ++j) {
             const int m = mbase + j;
-            if (m < M) tot[j] = __ldcg(wsl + j * BM);
+            if (m < M) {
+              tot[j] = __ldcg(wsl + j * BM);
+              __stcg(wsl + j * BM, 0);
+            }
           }
         }
       }
       if (finish) {
         const float swn = sw[n];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
+        for (int j = 0; j < HB; ++j) {
           const int m = mbase + j;
           if (m < M) {
             const size_t idx = static_cast<size_t>(m) * N + n;
@@ -554,9 +609,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
   }
 
   tc_fence_before();
+  // single-lane roles end at different times from the rest of their warp: the
+  // warp converges first so that the CTA barrier below waits for every thread
+  // (the tensor memory is released only after the last drain has read it)
+  __syncwarp();
   __syncthreads();
   if (warp == WARP_MMA) {
-    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
@@ -590,10 +648,15 @@ bool make_map_2d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, CUtens
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tokens per tile for a batch of M tokens: the narrowest MMA N that holds the
+// batch up to 64 tokens, 128 above.
+int tile_tokens(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128)); }
+
 // The schedule of a problem (see Work) on `grid` CTAs, and the workspace
 // bytes its split tiles need (0 when no tile is split).
 size_t plan_work(int M, int N, int K, int num_sms, Work* w, int* grid) {
-  w->mtiles = (M + BN - 1) / BN;
+  const int bn = tile_tokens(M);
+  w->mtiles = (M + bn - 1) / bn;
   w->chunks = K / kBlock;
   const int tiles = w->mtiles * (N / BM);
   if (tiles >= num_sms) {
@@ -614,37 +677,20 @@ size_t plan_work(int M, int N, int K, int num_sms, Work* w, int* grid) {
     w->tgrid = 0;
     return 0;
   }
-  return static_cast<size_t>(w->tail) * (BM * BN) * 4 + static_cast<size_t>(w->tail) * 4;
+  return static_cast<size_t>(w->tail) * (BM * bn) * 4 + static_cast<size_t>(w->tail) * 4;
 }
 
-}  // namespace
-
-size_t prefill_workspace_bytes(int M, int N, int K, int num_sms) {
-  Work w;
-  int grid = 0;
-  return plan_work(M, N, K, num_sms, &w, &grid);
-}
-
-bool prefill_split_required(int M, int N, int num_sms) {
-  return ((M + BN - 1) / BN) * (N / BM) < num_sms;
-}
-
-int launch_prefill(const PrefillArgs& a, int* status, cudaStream_t st, cudaError_t* cerr) {
-  *cerr = cudaSuccess;
+template <class C>
+int launch_cfg(const PrefillArgs& a, int num_sms, int* status, cudaStream_t st, cudaError_t* cerr) {
   auto enc = get_encode_fn();
   if (enc == nullptr) {
     *cerr = cudaErrorNotSupported;
     return TL_ECUDA;
   }
-  int dev = 0, num_sms = 0;
-  if ((*cerr = cudaGetDevice(&dev)) != cudaSuccess) return TL_ECUDA;
-  if ((*cerr = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return TL_ECUDA;
-
   const int G = a.K / kGroup;
   CUtensorMap mx, mp, mq;
   if (!make_map_2d(enc, &mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.xq, a.K, a.M,
-                   static_cast<uint64_t>(a.K) * 2, BOX_K, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                   static_cast<uint64_t>(a.K) * 2, BOX_K, C::BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_2d(enc, &mp, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.packed, a.K / 4, a.N,
                    static_cast<uint64_t>(a.K) / 4, BK / 4, BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_map_2d(enc, &mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.qT, a.N, G, static_cast<uint64_t>(a.N),
@@ -665,21 +711,52 @@ int launch_prefill(const PrefillArgs& a, int* status, cudaStream_t st, cudaError
       w.tgrid = 0;
       if (grid > w.full) grid = w.full;
     } else {
+      // the workspace is zero (zeroed by the caller once, and returned to zero
+      // by every call that completes); the no-alloc entry clears it anyway
       ws_acc = static_cast<int32_t*>(a.workspace);
       ws_cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(a.workspace) +
-                                      static_cast<size_t>(w.tail) * (BM * BN) * 4);
-      if ((*cerr = cudaMemsetAsync(a.workspace, 0, need, st)) != cudaSuccess) return TL_ECUDA;
+                                      static_cast<size_t>(w.tail) * (BM * C::BN) * 4);
+      if (a.clear_workspace &&
+          (*cerr = cudaMemsetAsync(a.workspace, 0, need, st)) != cudaSuccess)
+        return TL_ECUDA;
     }
   }
-  const size_t smem = Smem::total + 1024;
-  if ((*cerr = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const size_t smem = C::stotal + 1024;
+  if ((*cerr = cudaFuncSetAttribute(prefill_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(smem))) != cudaSuccess)
     return TL_ECUDA;
-  if ((*cerr = launch_pdl(prefill_kernel, dim3(grid), dim3(kThreads), smem, st, mx, mp, mq, a.sw,
-                          a.sx, a.M, a.N, w, a.y, a.y_dtype, a.acc_dbg, ws_acc, ws_cnt, status)) !=
-      cudaSuccess)
+  if ((*cerr = launch_pdl(prefill_kernel<C>, dim3(grid), dim3(C::kThreads), smem, st, mx, mp, mq,
+                          a.sw, a.sx, a.M, a.N, w, a.y, a.y_dtype, a.acc_dbg, ws_acc, ws_cnt,
+                          status)) != cudaSuccess)
     return TL_ECUDA;
   return TL_OK;
+}
+
+}  // namespace
+
+size_t prefill_workspace_bytes(int M, int N, int K, int num_sms) {
+  Work w;
+  int grid = 0;
+  return plan_work(M, N, K, num_sms, &w, &grid);
+}
+
+bool prefill_split_required(int M, int N, int num_sms) {
+  const int bn = tile_tokens(M);
+  return ((M + bn - 1) / bn) * (N / BM) < num_sms;
+}
+
+int launch_prefill(const PrefillArgs& a, int* status, cudaStream_t st, cudaError_t* cerr) {
+  *cerr = cudaSuccess;
+  int dev = 0, num_sms = 0;
+  if ((*cerr = cudaGetDevice(&dev)) != cudaSuccess) return TL_ECUDA;
+  if ((*cerr = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return TL_ECUDA;
+  switch (tile_tokens(a.M)) {
+    case 16: return launch_cfg<Cfg16>(a, num_sms, status, st, cerr);
+    case 32: return launch_cfg<Cfg32>(a, num_sms, status, st, cerr);
+    case 64: return launch_cfg<Cfg64>(a, num_sms, status, st, cerr);
+    default: return launch_cfg<Cfg128>(a, num_sms, status, st, cerr);
+  }
 }
 
 }  // namespace tl

@@ -148,7 +148,7 @@ int tl_linear_prefill(const uint8_t* packed, const int8_t* qT, const float* sw,
   if (workspace && !aligned16(workspace)) return TL_EINVAL;
   int* status = nullptr;
   if ((r = status_ptr(&status)) != TL_OK) return r;
-  tl::PrefillArgs a{packed, qT, sw, xq, sx, M, N, K, y, y_dtype, acc_dbg, workspace, ws_bytes};
+  tl::PrefillArgs a{packed, qT, sw, xq, sx, M, N, K, y, y_dtype, acc_dbg, workspace, ws_bytes, false};
   cudaError_t ce;
   return tl::launch_prefill(a, status, as_stream(stream), &ce);
 }
@@ -173,7 +173,7 @@ int tl_linear_prefill_noalloc(const uint8_t* packed, const int8_t* qT, const flo
   void* scratch = nullptr;
   if ((r = tl::prefill_noalloc_scratch(&scratch)) != TL_OK) return r;
   tl::PrefillArgs a{packed, qT, sw, xq, sx, M, N, K, y, y_dtype, acc_dbg, scratch,
-                    tl::kNoAllocScratchBytes};
+                    tl::kNoAllocScratchBytes, true};
   cudaError_t ce;
   return tl::launch_prefill(a, status, as_stream(stream), &ce);
 }

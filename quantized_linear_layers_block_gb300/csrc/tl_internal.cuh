@@ -47,6 +47,7 @@ struct PrefillArgs {
   int32_t* acc_dbg;
   void* workspace;
   size_t ws_bytes;
+  bool clear_workspace;   // zero the part of the workspace the call uses before the kernel
 };
 
 cudaError_t launch_pack(const int8_t* codes, const uint16_t* s, int N, int K, uint32_t* packed,
@@ -192,18 +193,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
-// 2-D tiled TMA load multicast to the CTAs of this cluster in `mask`: the data
-// lands at the same shared-memory offset in each of them and completes on the
-// mbarrier at the same offset in each of them.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, int x, int y,
-                                               uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "h"(mask)
-      : "memory");
-}
-
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -249,14 +238,6 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-// Arrive on the mbarrier at the same offset in every CTA of `mask` once all
-// prior tcgen05 operations of this thread have completed.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar), "h"(mask)
       : "memory");
 }
 // D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16 (fp16 inputs, fp32 accumulate).

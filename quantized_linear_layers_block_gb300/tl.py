@@ -313,7 +313,8 @@ class TernaryLinear:
         if need == 0:
             return None
         if self._ws is None or self._ws.numel() < need:
-            self._ws = torch.empty((need,), dtype=torch.uint8, device=self.device)
+            # zeroed once here; every call that completes leaves it zero again
+            self._ws = torch.zeros((need,), dtype=torch.uint8, device=self.device)
         return self._ws
 
     def forward(self, x: torch.Tensor, stream=None, out: torch.Tensor | None = None) -> torch.Tensor:

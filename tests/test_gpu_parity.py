@@ -91,6 +91,43 @@ def test_pack_flags_bad_codes(tl):
     assert tl.tl_get_status() == tl.TL_OK      # cleared by the read
 
 
+def test_weights_used_right_after_packing(tl):
+    """The GEMM kernels load weights before they wait on the preceding kernel;
+    tl_pack_weights' outputs are used by the very next launches on the same
+    stream, with no synchronisation in between, and must give the oracle's result."""
+    L = synth.config_inputs("decode", M=1, N=2048, K=5120)
+    r = O.layer(L.x_bits, L.codes, L.s)
+    codes = dev(L.codes)
+    s = dev(L.s.view(np.int16), torch.float16)
+    x = x_dev(L)
+    xq8, sx8 = tl.tl_rotate_quant_act(x, xq_dtype=tl.TL_I8)
+    xq16, sx16 = tl.tl_rotate_quant_act(x, xq_dtype=tl.TL_F16)
+    torch.cuda.synchronize()
+    N, K = L.N, L.K
+    packed = torch.empty((N, K // 4), dtype=torch.uint8, device="cuda")
+    qT = torch.empty((K // 128, N), dtype=torch.int8, device="cuda")
+    sw = torch.empty((N,), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    for path in ("fused", "decode", "prefill"):
+        for _ in range(3):
+            acc = torch.full((1, L.N), ACC_SENTINEL, dtype=torch.int32, device="cuda")
+            # stale contents that would give a different result if read early
+            packed.fill_(0x55)
+            qT.fill_(127)
+            sw.fill_(1.0)
+            assert tl.lib().tl_pack_weights(codes.data_ptr(), s.data_ptr(), N, K, packed.data_ptr(),
+                                            qT.data_ptr(), sw.data_ptr(), stream) == tl.TL_OK
+            # no synchronisation: the next launch on the stream consumes the weights
+            if path == "fused":
+                tl.tl_linear_decode_fused(packed, qT, sw, x, L.N, L.K, 4, acc_dbg=acc)
+            elif path == "decode":
+                tl.tl_linear_decode(packed, qT, sw, xq8, sx8, L.N, L.K, 4, acc_dbg=acc)
+            else:
+                tl.tl_linear_prefill(packed, qT, sw, xq16, sx16, L.N, L.K, 4, acc_dbg=acc)
+            check_status(tl)
+            assert np.array_equal(acc.cpu().numpy().astype(np.int64), r["acc"]), path
+
+
 # ------------------------------------------------------------------ K1 rotate + quantise
 
 def _rq_cases():
@@ -125,6 +162,54 @@ def test_rotate_quant_bitexact(tl, name, xb, signs):
     assert np.array_equal(sx2.cpu().numpy(), sx.cpu().numpy())
 
 
+def _tiny_tokens(K=2048):
+    """Tokens of bf16 subnormals whose largest rotated value is below 127 / FLT_MAX,
+    so that fl32(127 / a) overflows to +inf (the oracle's reading: non-zero
+    elements code to +-127, exact zeros to 0), next to an ordinary token."""
+    x = np.zeros((4, K), dtype=np.uint16)
+    x[0, 0], x[0, 1] = 0x0001, 0x0002            # two subnormals: +-127 over block 0, zeros after
+    x[1, 0] = 0x0001                             # one subnormal: block 0 all +127, the rest exact zeros
+    x[2] = synth.bf16_bits_from_f32(np.random.default_rng(5).standard_normal(K).astype(np.float32))
+    x[3, 3], x[3, K - 1] = 0x8005, 0x0003        # subnormals of both signs in the first and last block
+    return x
+
+
+def test_tiny_token_quantiser(tl):
+    """The subnormal-token case through K1 (int8 and fp16 images), the decode and
+    prefill GEMMs and the fused decode, bit-exact against the oracle."""
+    K, N = 2048, 256
+    xb = _tiny_tokens(K)
+    xq_ref, sx_ref = O.rotate_quant(xb)
+    assert np.any(sx_ref[[0, 1, 3]] < np.float32(1e-40))      # the overflow case is reached
+    xd = dev(xb.view(np.int16), torch.bfloat16)
+    xq, sx = tl.tl_rotate_quant_act(xd, xq_dtype=tl.TL_I8)
+    xh, sx2 = tl.tl_rotate_quant_act(xd, xq_dtype=tl.TL_F16)
+    check_status(tl)
+    assert np.array_equal(xq.cpu().numpy(), xq_ref)
+    assert np.array_equal(xh.cpu().numpy().astype(np.int64), xq_ref.astype(np.int64))
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), sx_ref.view(np.uint32))
+    assert np.array_equal(sx2.cpu().numpy().view(np.uint32), sx_ref.view(np.uint32))
+
+    L = synth.config_inputs("decode", M=4, N=N, K=K)
+    L.x_bits = xb
+    packed, qT, sw = pack_dev(tl, L)
+    r = O.layer(L.x_bits, L.codes, L.s)
+    for path in ("decode", "prefill"):
+        acc, y = _run(tl, path, L, packed, qT, sw, 4)
+        assert np.array_equal(acc.astype(np.int64), r["acc"]), path
+        assert np.array_equal(y.cpu().numpy().view(np.uint32), r["y32"].view(np.uint32)), path
+    for M in (1, 4):
+        acc = torch.full((M, N), ACC_SENTINEL, dtype=torch.int32, device="cuda")
+        xq1 = torch.zeros((M, K), dtype=torch.int8, device="cuda")
+        sx1 = torch.zeros((M,), dtype=torch.float32, device="cuda")
+        tl.tl_linear_decode_fused(packed, qT, sw, xd[:M].contiguous(), N, K, 4, acc_dbg=acc,
+                                  xq_out=xq1, sx_out=sx1)
+        check_status(tl)
+        assert np.array_equal(xq1.cpu().numpy(), xq_ref[:M])
+        assert np.array_equal(sx1.cpu().numpy().view(np.uint32), sx_ref[:M].view(np.uint32))
+        assert np.array_equal(acc.cpu().numpy().astype(np.int64), r["acc"][:M])
+
+
 # ------------------------------------------------------------------ K2 / K3 layer parity
 
 def _run(tl, path, L, packed, qT, sw, y_dtype):
@@ -137,7 +222,7 @@ def _run(tl, path, L, packed, qT, sw, y_dtype):
     else:
         xq, sx = tl.tl_rotate_quant_act(xd, xq_dtype=tl.TL_F16)
         need = tl.tl_prefill_workspace_size(M, L.N, L.K)
-        ws = torch.empty((max(need, 16),), dtype=torch.uint8, device="cuda") if need else None
+        ws = torch.zeros((max(need, 16),), dtype=torch.uint8, device="cuda") if need else None
         y = tl.tl_linear_prefill(packed, qT, sw, xq, sx, L.N, L.K, y_dtype, acc_dbg=acc, workspace=ws)
     check_status(tl)
     return acc.cpu().numpy(), y
@@ -292,7 +377,7 @@ def test_prefill_split_k_matches_unsplit(tl):
     xq, sx = tl.tl_rotate_quant_act(x_dev(L), xq_dtype=tl.TL_F16)
     need = tl.tl_prefill_workspace_size(L.M, L.N, L.K)
     assert need > 0
-    ws = torch.empty((need,), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros((need,), dtype=torch.uint8, device="cuda")
     a1 = torch.empty((L.M, L.N), dtype=torch.int32, device="cuda")
     a2 = torch.empty_like(a1)
     y1 = tl.tl_linear_prefill(packed, qT, sw, xq, sx, L.N, L.K, 4, acc_dbg=a1, workspace=ws)
@@ -300,6 +385,34 @@ def test_prefill_split_k_matches_unsplit(tl):
     check_status(tl)
     assert torch.equal(a1, a2) and torch.equal(y1, y2)
     _compare(L, a1.cpu().numpy(), y1, 4)
+    # the call returned the workspace to zero: the next call needs no clearing
+    assert not torch.any(ws)
+    a3 = torch.empty_like(a1)
+    tl.tl_linear_prefill(packed, qT, sw, xq, sx, L.N, L.K, 4, acc_dbg=a3, workspace=ws)
+    check_status(tl)
+    assert torch.equal(a3, a1) and not torch.any(ws)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 17408, 5120), (16, 5120, 17408), (9, 384, 2048),
+                                   (32, 17408, 5120), (20, 640, 8192), (64, 5120, 17408),
+                                   (48, 1152, 3072)])
+def test_prefill_narrow_tiles(tl, M, N, K):
+    """Batches of at most 16, 32 and 64 tokens run on tiles of that many tokens
+    (split along K where the tiles are fewer than the SMs): the int32 result
+    equals the oracle's on every row, the workspace is left zero, and the
+    128-token-tile kernel (a batch padded to 65 tokens) gives the same rows."""
+    L = synth.config_inputs("decode", M=M, N=N, K=K)
+    packed, qT, sw = pack_dev(tl, L)
+    rows = None if N <= 2048 else _sample_rows(N)
+    acc, y = _run(tl, "prefill", L, packed, qT, sw, 4)
+    _compare(L, acc, y, 4, rows=rows, frobenius=False)
+    xb = np.zeros((65, K), dtype=np.uint16)
+    xb[:M] = L.x_bits
+    xq, sx = tl.tl_rotate_quant_act(dev(xb.view(np.int16), torch.bfloat16), xq_dtype=tl.TL_F16)
+    a65 = torch.empty((65, N), dtype=torch.int32, device="cuda")
+    tl.tl_linear_prefill(packed, qT, sw, xq, sx, N, K, 4, acc_dbg=a65, workspace=None)
+    check_status(tl)
+    assert np.array_equal(a65[:M].cpu().numpy(), acc)
 
 
 def test_prefill_repeatable_after_sync(tl):

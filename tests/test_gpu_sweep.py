@@ -43,7 +43,7 @@ def test_sweep(name, M):
         if path == "prefill":
             xq, sx = tl.tl_rotate_quant_act(x, xq_dtype=tl.TL_F16)
             ws = tl.tl_prefill_workspace_size(M, N, K)
-            wsb = torch.empty((max(ws, 16),), dtype=torch.uint8, device="cuda")
+            wsb = torch.zeros((max(ws, 16),), dtype=torch.uint8, device="cuda")
             y = tl.tl_linear_prefill(packed, qT, sw, xq, sx, N, K, tl.TL_F32, acc_dbg=acc, workspace=wsb)
         else:
             xq, sx = tl.tl_rotate_quant_act(x, xq_dtype=tl.TL_I8)

@@ -15,6 +15,7 @@ the CPU mock: 2.6e-3 vs TP=1, 1.44 with ranks swapped), §4 "効いた高速化"
 
 import json
 import os
+import warnings
 
 import numpy as np
 import pytest
@@ -23,7 +24,8 @@ import scipy.linalg
 from oracle import ternary_linear as O
 from quantized_linear_layers_block_gb300 import synth
 
-pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+# a pin that overflows or divides by zero somewhere unplanned fails loudly
+pytestmark = pytest.mark.filterwarnings("error::RuntimeWarning")
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -168,6 +170,44 @@ def pin_quant_properties():
         assert np.all(err <= 0.5 * float(sx[m]) * (1 + 1e-5))
 
 
+def pin_quant_tiny_token():
+    """Hand-derived: tokens of bf16 subnormals, where fl32(127 / a) overflows to +inf.
+
+    Token 0: x[0] = 2^-133 (bf16 bits 0x0001), x[1] = 2^-132 (0x0002), zero
+    elsewhere, K = 2048. Block 0 rotates to (2^-133 + 2^-132) / 32 = 3 2^-138 at
+    even i and (2^-133 - 2^-132) / 32 = -2^-138 at odd i, all exact fp32
+    subnormals; block 1 is zero. a = 3 2^-138 < 127 / FLT_MAX, so inv = +inf:
+    block 0 codes to +127 / -127 (even / odd i), block 1's zeros to 0, and
+    sx = fl32(3 2^-138 / 127) = 48 2^-149 (3 2^11 / 127 = 48.38 rounds to 48).
+    Token 1: x[0] = 2^-133 alone: block 0 is 2^-138 everywhere -> +127,
+    block 1 -> 0, sx = fl32(2^-138 / 127) = 16 2^-149 (2^11 / 127 = 16.13).
+    """
+    x = np.zeros((2, 2048), dtype=np.uint16)
+    x[0, 0], x[0, 1] = 0x0001, 0x0002
+    x[1, 0] = 0x0001
+    xr = O.rotate_fp32(x)
+    tiny = np.float32(2.0 ** -138)
+    assert np.all(xr[0, 0:1024:2] == np.float32(3) * tiny)
+    assert np.all(xr[0, 1:1024:2] == -tiny) and not np.any(xr[0, 1024:])
+    with np.errstate(over="ignore"):
+        assert np.float32(127) / (np.float32(3) * tiny) == np.inf
+    xq, sx = O.quantize_per_token(xr)
+    want0 = np.zeros(2048, dtype=np.int64)
+    want0[0:1024:2], want0[1:1024:2] = 127, -127
+    want1 = np.zeros(2048, dtype=np.int64)
+    want1[:1024] = 127
+    assert np.array_equal(xq[0].astype(np.int64), want0)
+    assert np.array_equal(xq[1].astype(np.int64), want1)
+    assert sx[0] == np.float32(48 * 2.0 ** -149) and sx[1] == np.float32(16 * 2.0 ** -149)
+    # the boundary: just above 127 / FLT_MAX the quotient is finite and the
+    # ordinary rule applies (one element reaches 127, the half-ulp bound holds)
+    a = np.float32(np.float32(127) / np.finfo(np.float32).max)
+    a_up = np.nextafter(np.nextafter(a, np.float32(1)), np.float32(1))
+    xr2 = np.array([[a_up, -a_up / 2, 0, a_up / 4] + [0] * 1020], dtype=np.float32)
+    xq2, sx2 = O.quantize_per_token(xr2)
+    assert xq2[0, :4].tolist() == [127, -64, 0, 32]
+
+
 def pin_pack_layout_handworked():
     """One 16-code word worked by hand (layout: field at bit 16h+2j holds code[2j+h]+1).
 
@@ -287,7 +327,8 @@ def pin_layer_error_level():
 
 PINS = [pin_hadamard, pin_fwht_vs_library, pin_sylvester_recursion, pin_rank_swap_control,
         pin_tp_split_bf16_level, pin_rotation_orthonormal, pin_rotate_fp32_near_fp64,
-        pin_quant_one_hot, pin_quant_properties, pin_pack_layout_handworked, pin_pack_roundtrip,
+        pin_quant_one_hot, pin_quant_properties, pin_quant_tiny_token,
+        pin_pack_layout_handworked, pin_pack_roundtrip,
         pin_row_scale_decompose, pin_int_gemm_bruteforce, pin_int_gemm_extremes,
         pin_epilogue_closed_form, pin_layer_one_hot_exact, pin_layer_error_level]
 
@@ -334,6 +375,16 @@ def _quant_128(xr):
     return xq, (a / np.float32(128)).astype(np.float32)
 
 
+def _quant_nan_unhandled(xr):
+    xr = np.asarray(xr, dtype=np.float32)
+    a = np.max(np.abs(xr), axis=1)
+    inv = (np.float32(127) / a).astype(np.float32)
+    t = xr * inv[:, None]
+    # planted: NaN (0 * inf) left to the int8 cast, +-inf clamped, as a naive port would
+    xq = np.clip(np.rint(np.nan_to_num(t, nan=127.0)), -127, 127).astype(np.int8)
+    return xq, (a / np.float32(127)).astype(np.float32)
+
+
 def _decompose_no_abs(s):
     sf = np.asarray(s, dtype=np.float16).astype(np.float32)
     smax = np.max(sf, axis=1)                                # planted: max without |.|
@@ -362,6 +413,7 @@ MUTATIONS = [
     ("expand_w_int8", _expand_shifted_group, [pin_int_gemm_bruteforce]),
     ("expand_w_int8", _expand_rows_reversed, [pin_int_gemm_bruteforce]),
     ("quantize_per_token", _quant_128, [pin_quant_one_hot]),
+    ("quantize_per_token", _quant_nan_unhandled, [pin_quant_tiny_token]),
     ("row_scale_decompose", _decompose_no_abs, [pin_row_scale_decompose]),
     ("pack_codes", _pack_swapped_halves, [pin_pack_layout_handworked]),
     ("epilogue", _epilogue_no_token_scale, [pin_epilogue_closed_form]),
@@ -374,10 +426,12 @@ def test_planted_mistake_is_caught(monkeypatch, name, fake, pins):
     monkeypatch.setattr(O, name, fake)
     caught = []
     for pin in pins:
-        try:
-            pin()
-        except (AssertionError, ValueError, IndexError):
-            caught.append(pin.__name__)
+        with warnings.catch_warnings():
+            warnings.simplefilter("ignore", RuntimeWarning)   # the planted versions may overflow
+            try:
+                pin()
+            except (AssertionError, ValueError, IndexError):
+                caught.append(pin.__name__)
     assert caught, f"no pin caught the planted mistake in {name}"
 
 

@@ -45,7 +45,7 @@ def test_noalloc_matches_workspace_version_on_two_calls(tl):
     packed, qT, sw = tl.tl_pack_weights(_dev(L.codes), _dev(L.s.view(np.int16), torch.float16))
     x = _dev(L.x_bits.view(np.int16), torch.bfloat16)
     xq, sx = tl.tl_rotate_quant_act(x, xq_dtype=tl.TL_F16)
-    ws = torch.empty((need,), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros((need,), dtype=torch.uint8, device="cuda")
     acc_ref = torch.empty((L.M, L.N), dtype=torch.int32, device="cuda")
     y_ref = tl.tl_linear_prefill(packed, qT, sw, xq, sx, L.N, L.K, tl.TL_F32, acc_dbg=acc_ref,
                                  workspace=ws)
@@ -60,33 +60,87 @@ def test_noalloc_matches_workspace_version_on_two_calls(tl):
         assert err <= FP32_TOL
 
 
-def test_noalloc_refuses_problems_beyond_its_scratch(tl):
-    limit = 8 * 1024 * 1024
-    shape = None
-    for M in (1024, 2048, 4096, 8192):
-        for N in (1152, 2304, 4608):
-            if tl.tl_prefill_workspace_size(M, N, 17408) > limit:
-                shape = (M, N)
-                break
-        if shape:
-            break
-    if shape is None:
-        pytest.skip("no shape on this device needs more split-K scratch than the array holds")
-    M, N = shape
-    K = 2048   # the refusal happens before any launch; keep the buffers small
-    if tl.tl_prefill_workspace_size(M, N, K) <= limit:
-        K = 17408
-    packed = torch.zeros((N, K // 4), dtype=torch.uint8, device="cuda")
-    qT = torch.zeros((K // 128, N), dtype=torch.int8, device="cuda")
-    sw = torch.zeros((N,), dtype=torch.float32, device="cuda")
-    xq = torch.zeros((M, K), dtype=torch.float16, device="cuda")
-    sx = torch.zeros((M,), dtype=torch.float32, device="cuda")
-    y = torch.full((M, N), 7.0, dtype=torch.float32, device="cuda")
+LIMIT = 8 * 1024 * 1024
+M_TILE = 128      # a 128-token batch runs on one 128-token tile; its split-K slot is 64 KB
+
+
+def _sms():
+    return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+
+
+def _zeros_layer(M, N, K):
+    return (torch.zeros((N, K // 4), dtype=torch.uint8, device="cuda"),
+            torch.zeros((K // 128, N), dtype=torch.int8, device="cuda"),
+            torch.zeros((N,), dtype=torch.float32, device="cuda"),
+            torch.zeros((M, K), dtype=torch.float16, device="cuda"),
+            torch.zeros((M,), dtype=torch.float32, device="cuda"))
+
+
+def _call_raw(tl, packed, qT, sw, xq, sx, M, N, K, y, acc=None):
     P = ctypes.c_void_p
-    rc = tl.lib().tl_linear_prefill_noalloc(P(packed.data_ptr()), P(qT.data_ptr()), P(sw.data_ptr()),
-                                           P(xq.data_ptr()), P(sx.data_ptr()), M, N, K,
-                                           P(y.data_ptr()), tl.TL_F32, None,
-                                           P(torch.cuda.current_stream().cuda_stream))
-    assert rc == tl.TL_ENOSPACE
+    return tl.lib().tl_linear_prefill_noalloc(P(packed.data_ptr()), P(qT.data_ptr()), P(sw.data_ptr()),
+                                             P(xq.data_ptr()), P(sx.data_ptr()), M, N, K,
+                                             P(y.data_ptr()), tl.TL_F32,
+                                             None if acc is None else P(acc.data_ptr()),
+                                             P(torch.cuda.current_stream().cuda_stream))
+
+
+def test_noalloc_allocates_nothing(tl):
+    """After a first call (which loads the kernels), a call changes neither the
+    caching allocator's bytes nor the device's free memory."""
+    L = synth.config_inputs("down_proj", M=64, N=256, K=17408)
+    packed, qT, sw = tl.tl_pack_weights(_dev(L.codes), _dev(L.s.view(np.int16), torch.float16))
+    xq, sx = tl.tl_rotate_quant_act(_dev(L.x_bits.view(np.int16), torch.bfloat16), xq_dtype=tl.TL_F16)
+    y = torch.empty((L.M, L.N), dtype=torch.float32, device="cuda")
+    acc = torch.empty((L.M, L.N), dtype=torch.int32, device="cuda")
+    assert _call_raw(tl, packed, qT, sw, xq, sx, L.M, L.N, L.K, y, acc) == tl.TL_OK
+    torch.cuda.synchronize()
+    first = acc.clone()
+    free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+    for _ in range(3):
+        assert _call_raw(tl, packed, qT, sw, xq, sx, L.M, L.N, L.K, y, acc) == tl.TL_OK
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == alloc0
+    assert torch.cuda.mem_get_info()[0] >= free0
+    assert tl.tl_get_status() == tl.TL_OK
+    assert torch.equal(acc, first)
+
+
+def test_noalloc_refuses_problems_beyond_its_scratch(tl):
+    """Fewer tiles than SMs (K must be split) and more split-K scratch than the
+    array holds: refused before any launch."""
+    sms = _sms()
+    M, K = M_TILE, 2048
+    # the most 128-row tiles below the SM count: all of them are cut along K
+    N = (sms - 1) * 128
+    need = tl.tl_prefill_workspace_size(M, N, K)
+    if need <= LIMIT:
+        pytest.skip(f"with {sms} SMs no single-tile-row problem needs more than the array holds")
+    assert (N // 128) < sms
+    packed, qT, sw, xq, sx = _zeros_layer(M, N, K)
+    y = torch.full((M, N), 7.0, dtype=torch.float32, device="cuda")
+    assert _call_raw(tl, packed, qT, sw, xq, sx, M, N, K, y) == tl.TL_ENOSPACE
     assert tl.tl_get_status() == tl.TL_OK
     assert torch.all(y == 7.0)
+
+
+def test_noalloc_runs_unsplit_when_tiles_fill_the_gpu(tl):
+    """At least as many tiles as SMs: only the last partial round would be split;
+    when its scratch does not fit, every tile runs whole and the result is the
+    same as tl_linear_prefill's."""
+    sms = _sms()
+    M, K = M_TILE, 2048
+    N = (sms + 140) * 128          # one full round, then 140 tiles left over (> 128 slots of 64 KB)
+    need = tl.tl_prefill_workspace_size(M, N, K)
+    assert (N // 128) >= sms and need > LIMIT
+    L = synth.config_inputs("gate_up", M=M, N=N, K=K)
+    packed, qT, sw = tl.tl_pack_weights(_dev(L.codes), _dev(L.s.view(np.int16), torch.float16))
+    xq, sx = tl.tl_rotate_quant_act(_dev(L.x_bits.view(np.int16), torch.bfloat16), xq_dtype=tl.TL_F16)
+    acc_ref = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    ws = torch.zeros((need,), dtype=torch.uint8, device="cuda")
+    tl.tl_linear_prefill(packed, qT, sw, xq, sx, N, K, tl.TL_F32, acc_dbg=acc_ref, workspace=ws)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    acc = torch.full((M, N), -(2 ** 31), dtype=torch.int32, device="cuda")
+    assert _call_raw(tl, packed, qT, sw, xq, sx, M, N, K, y, acc) == tl.TL_OK
+    assert tl.tl_get_status() == tl.TL_OK
+    assert torch.equal(acc, acc_ref)
