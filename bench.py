@@ -41,13 +41,13 @@ LAYERS = 64
 PREFILL = dict(name="gate_up", M=512, K=5120, N=34816)
 DECODE = dict(name="decode", M=1, K=5120, N=17408)
 METRIC = "ternary linear int8 TOPS @M=512; decode GEMV weight-stream GB/s @M=1"
+CONFIG_SWEEP_M = (1, 4, 16, 64, 256, 1024, 4096)   # the M-sweep points reported in `configs`
 CONFIG = {
     "workload": "prefill fused gate+up M=512 K=5120 N=34816, one step = 64 layer buffers; "
                 "decode M=1 K=5120 N=17408, one step = 64 layer buffers",
     "layers_per_step": LAYERS,
     "l2": "inputs larger than L2: 64 distinct layer buffers (2.95 GB prefill, 1.47 GB decode weights)",
 }
-DP4A_PER_CLK_SM = 60.0    # dp4a lane-ops per clock per SM, measured on GB300 (independent chains)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -257,6 +257,8 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="layer buffers per step (64 = the model's depth; fewer only for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload kernel times (down_proj M=256, the M-sweep subset)")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the benchmark line: the M sweep 1..4096 over both MLP shapes, "
                          "one JSON line per point (prefill kernel, and decode kernel for M <= 32)")
@@ -343,8 +345,8 @@ def main(argv=None):
         lay, x, y = dec_layers[li]
         tl.tl_linear_decode_fused(lay.packed, lay.qT, lay.sw, x, D["N"], D["K"], tl.TL_BF16, y=y)
 
-    # M = 16 at the decode shape: the whole layer as TernaryLinear runs it (M*K > 72K: K1 with
-    # the fp16 image, then the tensor-core kernel), and that kernel alone
+    # M = 16 at the decode shape: the whole layer as TernaryLinear runs it (K1 with the fp16
+    # image, then the mma.sync tensor-core decode), and that kernel alone
     M16 = 16
     _, _, x16 = synth.torch_config_layer(D["name"], 0, M=M16, device=str(dev))
     y16 = torch.empty((M16, D["N"]), dtype=torch.bfloat16, device=dev)
@@ -356,10 +358,16 @@ def main(argv=None):
     def layer16(li):
         dec_layers[li][0].forward(x16, out=y16)
 
+    kind16 = dec_layers[0][0].kernel_for(M16)
+
     def kernel16(li):
         lay = dec_layers[li][0]
-        tl.tl_linear_prefill(lay.packed, lay.qT, lay.sw, xq16, sx16, D["N"], D["K"], tl.TL_BF16,
-                             y=y16, workspace=ws16)
+        if kind16 == "decode_tc":
+            tl.tl_linear_decode_tc(lay.packed, lay.qT, lay.sw, xq16, sx16, D["N"], D["K"],
+                                   tl.TL_BF16, y=y16)
+        else:
+            tl.tl_linear_prefill(lay.packed, lay.qT, lay.sw, xq16, sx16, D["N"], D["K"], tl.TL_BF16,
+                                 y=y16, workspace=ws16)
 
     # warm-up (also resolves driver entry points and kernel attributes before capture)
     for _ in range(args.warmup):
@@ -510,6 +518,18 @@ def main(argv=None):
         dstep.run()
     e2e_dec_s = max(max_over_ranks(time.perf_counter() - t0), 1e-9)
 
+    # ---------------- the other workloads: down_proj at 256 tokens and a subset of the M sweep
+    # over both MLP shapes (kernel time per layer, 8 layer buffers each, outside the timed steps)
+    peaks0, _ = load_peaks()
+    configs = None
+    if not args.no_configs:
+        configs = time_points(tl, synth, dev, stream,
+                              [("down_proj", 256)] + [(nm, m) for nm in ("sweep_up", "sweep_down")
+                                                      for m in CONFIG_SWEEP_M],
+                              hbm_peak=float(peaks0.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
+                              tc_peak=float(peaks0.get("bf16_tflops_sustained",
+                                                       FALLBACK_PEAKS["bf16_tflops_sustained"])))
+
     # ---------------- figures
     flop_layer = 2.0 * P["M"] * P["N"] * P["K"]
     tops = ws * K * LAYERS * flop_layer / (pre_ms * 1e-3) / 1e12
@@ -523,8 +543,6 @@ def main(argv=None):
     k2_gbs = dec_alg_bytes / (k2_ms * 1e-3) / 1e9
     traffic = _profiled_traffic()
     flop16 = 2.0 * 16 * D["N"] * D["K"]
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    alu_peak = 8 * DP4A_PER_CLK_SM * sms * float(clk.get("sm_mhz") or 2070.0) * 1e6 / 1e12
 
     line = {
         "metric": METRIC, "value": tops, "unit": "TOPS", "n_gpus": ws, "steps": K,
@@ -557,14 +575,15 @@ def main(argv=None):
             "metric": "ternary linear int8 TOPS @M=16, decode shape (K=5120, N=17408)",
             "value": flop16 / (m16_layer_us * 1e-6) / 1e12, "unit": "TOPS",
             "layer_us": m16_layer_us, "kernel_us": m16_kernel_us,
-            "kernel": "prefill_kernel (K3), TernaryLinear's choice for M*K > 72K; 64 layer buffers "
-                      "in a CUDA graph",
-            "roofline": {"bound": "alu", "achieved": flop16 / (m16_kernel_us * 1e-6) / 1e12,
-                         "peak": alu_peak, "unit": "TOPS",
-                         "frac": flop16 / (m16_kernel_us * 1e-6) / 1e12 / alu_peak,
-                         "peak_source": "the dp4a decode path's ceiling: 60 dp4a lane-ops per clock "
-                                        "per SM (measured with a probe of independent dp4a chains) "
-                                        "x 8 int8 ops x SMs x the median SM clock sampled here"},
+            "kernel": f"{kind16} (TernaryLinear's choice for M = 16 at K = 5120); 64 layer "
+                      "buffers in a CUDA graph",
+            # the operation at M = 16 moves 23 MB of weights for 2.85 GOP: HBM-bound against
+            # the measured peaks (the weight stream takes longer than the tensor work)
+            "roofline": {"bound": "hbm", "achieved": wb / (m16_kernel_us * 1e-6) / 1e9,
+                         "peak": hbm_peak, "unit": "GB/s",
+                         "frac": wb / (m16_kernel_us * 1e-6) / 1e9 / hbm_peak,
+                         "peak_source": f"{peak_src} hbm_gbs",
+                         "floor_us": wb / hbm_peak / 1e3},
         },
         "decode_f32act": {
             "metric": "float-activation decode GEMV weight-stream GB/s @M=1",
@@ -576,6 +595,7 @@ def main(argv=None):
                     "64 layer buffers in a CUDA graph",
         },
         "codec": codec,
+        "configs": configs,
         "gpu_launches": K * LAYERS * 2 + Kd * LAYERS * 2,
         "clocks": clk,
     }
@@ -594,11 +614,86 @@ def main(argv=None):
     return 0
 
 
+def time_points(tl, synth, dev, stream, points, nl: int = 8, hbm_peak=None, tc_peak=None) -> list:
+    """Kernel time per layer of named workloads at given token counts.
+
+    points: (workload name, M) pairs. For each workload `nl` layer buffers
+    (larger than L2 together) are drawn with its recipe; for each M the kernel
+    TernaryLinear picks runs over the buffers in a CUDA graph (rotate+quantise
+    outside the timed launches), and the prefill kernel beside it when that is
+    not the one picked. Returns one dict per point with the times, TOPS,
+    weight GB/s and the roofline of the picked kernel: HBM-bound below the
+    M where the weight stream and the tensor work take equally long at the
+    measured peaks, tensor-bound above."""
+    import torch
+    out = []
+    cache = {}
+    for name, M in points:
+        if name not in cache:
+            cache.clear()
+            layers = []
+            for li in range(nl):
+                codes, s_, _ = synth.torch_config_layer(name, li, M=1, device=str(dev))
+                layers.append(tl.TernaryLinear(codes, s_, device=dev))
+                del codes, s_
+            cache[name] = layers
+        layers = cache[name]
+        N, K = layers[0].N, layers[0].K
+        _, _, x = synth.torch_config_layer(name, 1000, M=M, device=str(dev))
+        xq16, sx = tl.tl_rotate_quant_act(x, xq_dtype=tl.TL_F16)
+        xq8, _ = tl.tl_rotate_quant_act(x, xq_dtype=tl.TL_I8)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        ws = layers[0]._workspace(M)
+        fns = {
+            "prefill": lambda l: tl.tl_linear_prefill(l.packed, l.qT, l.sw, xq16, sx, N, K, tl.TL_BF16,
+                                                      y=y, workspace=ws),
+            "decode": lambda l: tl.tl_linear_decode(l.packed, l.qT, l.sw, xq8, sx, N, K, tl.TL_BF16, y=y),
+            "decode_tc": lambda l: tl.tl_linear_decode_tc(l.packed, l.qT, l.sw, xq16, sx, N, K,
+                                                          tl.TL_BF16, y=y),
+        }
+        picked = layers[0].kernel_for(M)
+        kinds = [picked] + (["prefill"] if picked != "prefill" else [])
+        wb = weight_bytes(N, K)
+        line = {"workload": name, "M": M, "K": K, "N": N, "kernel": picked}
+        for kind in kinds:
+            fn = fns[kind]
+            for l in layers:
+                fn(l)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()          # no host launch cost between the kernels
+            with torch.cuda.graph(g, capture_error_mode="relaxed"):
+                for l in layers:
+                    fn(l)
+            g.replay()
+            torch.cuda.synchronize()
+            reps = max(3, min(40, int(4e5 // max(M, 64))))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us = 1e3 * e0.elapsed_time(e1) / (reps * nl)
+            key = "us" if kind == picked else f"{kind}_us"
+            line[key] = round(us, 2)
+            if kind == picked:
+                line["tops"] = round(2.0 * M * N * K / (us * 1e-6) / 1e12, 1)
+                line["weight_GB/s"] = round(wb / (us * 1e-6) / 1e9, 1)
+                if hbm_peak and tc_peak:
+                    flops = 2.0 * M * N * K
+                    if wb / (hbm_peak * 1e9) >= flops / (tc_peak * 1e12):
+                        line["roofline"] = {"bound": "hbm", "frac": round(wb / (us * 1e-6) / 1e9 / hbm_peak, 3)}
+                    else:
+                        line["roofline"] = {"bound": "tensor",
+                                            "frac": round(flops / (us * 1e-6) / 1e12 / tc_peak, 3)}
+        if tl.tl_get_status() != tl.TL_OK:
+            raise RuntimeError(f"device status during {name} M={M}")
+        out.append(line)
+    return out
+
+
 def sweep_main(args) -> int:
-    """The M sweep of the workloads: for each MLP shape 8 layer buffers (larger
-    than L2 together), and for each M the prefill kernel (and, for M <= 32, the
-    decode kernel) over the buffers, captured in a CUDA graph and timed with
-    CUDA events; rotate+quantise is outside the timed launches."""
+    """The M sweep of the workloads (one JSON line per point; see time_points)."""
     import torch
     import __graft_entry__
     __graft_entry__.build()
@@ -606,50 +701,13 @@ def sweep_main(args) -> int:
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
-    nl = 8
-    for name in ("sweep_up", "sweep_down"):
-        K, N = synth.CONFIGS[name]["K"], synth.CONFIGS[name]["N"]
-        layers = []
-        for li in range(nl):
-            codes, s, _ = synth.torch_config_layer(name, li, M=1, device=str(dev))
-            layers.append(tl.TernaryLinear(codes, s, device=dev))
-            del codes, s
-        for M in synth.SWEEP_M:
-            x = torch.randn((M, K), device=dev).to(torch.bfloat16)
-            xq16, sx = tl.tl_rotate_quant_act(x, xq_dtype=tl.TL_F16)
-            xq8, _ = tl.tl_rotate_quant_act(x, xq_dtype=tl.TL_I8)
-            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-            ws = layers[0]._workspace(M)
-            runs = {"prefill": lambda l: tl.tl_linear_prefill(l.packed, l.qT, l.sw, xq16, sx, N, K, tl.TL_BF16,
-                                                              y=y, workspace=ws)}
-            if M <= 32:
-                runs["decode"] = lambda l: tl.tl_linear_decode(l.packed, l.qT, l.sw, xq8, sx, N, K, tl.TL_BF16, y=y)
-            line = {"shape": f"K={K} N={N}", "M": M}
-            for kind, fn in runs.items():
-                for l in layers:
-                    fn(l)
-                torch.cuda.synchronize()
-                g = torch.cuda.CUDAGraph()          # no host launch cost between the kernels
-                with torch.cuda.graph(g, capture_error_mode="relaxed"):
-                    for l in layers:
-                        fn(l)
-                g.replay()
-                torch.cuda.synchronize()
-                reps = max(3, min(40, int(4e5 // max(M, 64))))
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                for _ in range(reps):
-                    g.replay()
-                e1.record(stream)
-                torch.cuda.synchronize()
-                us = 1e3 * e0.elapsed_time(e1) / (reps * nl)
-                line[f"{kind}_us"] = round(us, 2)
-                line[f"{kind}_tops"] = round(2.0 * M * N * K / (us * 1e-6) / 1e12, 1)
-                if M == 1:
-                    line[f"{kind}_weight_GB/s"] = round(weight_bytes(N, K) / (us * 1e-6) / 1e9, 1)
-            if tl.tl_get_status() != tl.TL_OK:
-                raise RuntimeError("device status during the sweep")
-            print(json.dumps(line), flush=True)
+    peaks, _ = load_peaks()
+    points = [(name, M) for name in ("sweep_up", "sweep_down") for M in synth.SWEEP_M]
+    for line in time_points(tl, synth, dev, stream, points,
+                            hbm_peak=float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
+                            tc_peak=float(peaks.get("bf16_tflops_sustained",
+                                                    FALLBACK_PEAKS["bf16_tflops_sustained"]))):
+        print(json.dumps(line), flush=True)
     return 0
 
 

@@ -112,7 +112,8 @@ int tl_pack_weights(const int8_t* codes, const uint16_t* s, int N, int K,
  *             (NULL = all +1)
  *   xq        out [M, K]: the int8 codes; xq_dtype = TL_I8 stores int8 (the
  *             decode path's operand), TL_F16 stores the same integers as
- *             exact fp16 values (the prefill path's tensor-core operand)
+ *             exact fp16 values (the tensor-core operand of tl_linear_prefill
+ *             and tl_linear_decode_tc)
  *   sx        out fp32 [M]
  * Per token: xr = fl32 butterflies with strides 1,2,...,512 then x 1/32;
  * a = max |xr|; inv = fl32(127/a); xq = clamp(rne(fl32(xr inv)), +-127);
@@ -182,6 +183,26 @@ int tl_linear_prefill(const uint8_t* packed, const int8_t* qT, const float* sw,
 int tl_linear_decode(const uint8_t* packed, const int8_t* qT, const float* sw,
                      const int8_t* xq, const float* sx, int M, int N, int K,
                      void* y, int y_dtype, int32_t* acc_dbg, void* stream);
+
+/*
+ * Decode (1 <= M <= 32) ternary linear layer on the tensor cores: the same
+ * quantised layer (Qiita item ecc183fae033565af7cb §4 "効いた高速化") as
+ * tl_linear_decode and tl_linear_prefill, bit for bit, for the decode batch
+ * sizes of §5 "効かなかったもの" (the decode GEMV), as mma.sync.m16n8k16 with
+ * fp16 operands: each packed word's codes become the fp16 pairs code q exactly
+ * (the prefill's expansion, in registers), every 1024-column chunk is summed
+ * in fp32 (integers below 2^24, exact) and the chunks in int32.
+ *
+ *   packed, qT, sw   from tl_pack_weights
+ *   xq               fp16 [M, K] holding the int8 codes (tl_rotate_quant_act
+ *                    with TL_F16, as for tl_linear_prefill); sx fp32 [M]
+ *   y, y_dtype, acc_dbg   as for tl_linear_prefill
+ * M > 32 returns TL_EUNSUPPORTED. The weights are read before the wait on the
+ * preceding kernel (see the conventions above).
+ */
+int tl_linear_decode_tc(const uint8_t* packed, const int8_t* qT, const float* sw,
+                        const uint16_t* xq, const float* sx, int M, int N, int K, void* y,
+                        int y_dtype, int32_t* acc_dbg, void* stream);
 
 /*
  * Decode with the input-side rotation and per-token quantisation done inside

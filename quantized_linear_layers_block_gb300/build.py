@@ -22,7 +22,7 @@ CSRC = os.path.join(PKG, "csrc")
 OBJDIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libtl_gb300.so")
 SOURCES = ["tl_api.cu", "pack.cu", "rotate_quant.cu", "decode.cu", "decode_fused_m.cu", "prefill.cu", "codec.cu",
-           "decode_f32.cu"]
+           "decode_f32.cu", "decode_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", os.path.join(ROOT, "include")]
 

@@ -191,6 +191,21 @@ int tl_linear_decode(const uint8_t* packed, const int8_t* qT, const float* sw, c
              : TL_ECUDA;
 }
 
+int tl_linear_decode_tc(const uint8_t* packed, const int8_t* qT, const float* sw,
+                        const uint16_t* xq, const float* sx, int M, int N, int K, void* y,
+                        int y_dtype, int32_t* acc_dbg, void* stream) {
+  int r = check_linear(packed, qT, sw, xq, sx, M, N, K, y, y_dtype, acc_dbg);
+  if (r != TL_OK) return r;
+  if (M > tl::kMaxDecodeM) return TL_EUNSUPPORTED;
+  if (M == 0 || N == 0) return TL_OK;
+  int* status = nullptr;
+  if ((r = status_ptr(&status)) != TL_OK) return r;
+  return tl::launch_decode_tc(packed, qT, sw, xq, sx, M, N, K, y, y_dtype, acc_dbg, status,
+                              as_stream(stream)) == cudaSuccess
+             ? TL_OK
+             : TL_ECUDA;
+}
+
 int tl_linear_decode_fused(const uint8_t* packed, const int8_t* qT, const float* sw,
                            const uint16_t* x, const int8_t* signs, int M, int N, int K, void* y,
                            int y_dtype, int32_t* acc_dbg, int8_t* xq_out, float* sx_out,

@@ -7,6 +7,8 @@
 #include <cstdint>
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "../../include/tl.h"
@@ -90,6 +92,18 @@ int launch_prefill(const PrefillArgs& a, int* status, cudaStream_t st, cudaError
 // Device address (this device) of the library-owned split-K scratch array of
 // kNoAllocScratchBytes; the first call on a device looks it up.
 int prefill_noalloc_scratch(void** ptr);
+
+// cuTensorMapEncodeTiled from the driver (nullptr if unavailable), and a 2-D
+// tiled tensor map over a row-major array of `outer` rows of `row_bytes`.
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn();
+bool make_map_2d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, CUtensorMapDataType dt,
+                 const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                 uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz);
+
+// Tensor-core decode (1 <= M <= 32; xq the fp16 image of the int8 codes, [M, K]).
+cudaError_t launch_decode_tc(const uint8_t* packed, const int8_t* qT, const float* sw,
+                             const uint16_t* xq, const float* sx, int M, int N, int K, void* y,
+                             int y_dtype, int32_t* acc_dbg, int* status, cudaStream_t st);
 
 // Launch with programmatic stream serialization (PDL) enabled and, when
 // cluster > 1, thread-block clusters of `cluster` CTAs along x.
@@ -386,6 +400,29 @@ __device__ __forceinline__ float rotate_block_warp(const uint16_t* __restrict__ 
     }
   }
   return amax;
+}
+
+// Expand one packed word (16 codes, layout of tl.h) into 8 fp16 pairs code*q.
+// The 2-bit field e (= code + 1) is dropped into the mantissa of an fp16 whose
+// exponent makes the value 2^E + e exactly; subtracting 2^E + 1 leaves the code
+// in {-1, 0, +1} and one multiply by q gives code * q, all exact.
+__device__ __forceinline__ void expand_word(uint32_t w, __half2 q2, uint32_t* out) {
+  const __half2 c0 = __halves2half2(__ushort_as_half(0x6401), __ushort_as_half(0x6401));  // 1025
+  const __half2 c1 = __halves2half2(__ushort_as_half(0x5C04), __ushort_as_half(0x5C04));  // 257
+  const __half2 c2 = __halves2half2(__ushort_as_half(0x5410), __ushort_as_half(0x5410));  // 65
+  const __half2 c3 = __halves2half2(__ushort_as_half(0x4C40), __ushort_as_half(0x4C40));  // 17
+  const __half2 c4 = __halves2half2(__ushort_as_half(0x4500), __ushort_as_half(0x4500));  // 5
+  const __half2 cs[5] = {c0, c1, c2, c3, c4};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int jj = j < 5 ? j : j - 5;
+    const uint32_t src = j < 5 ? w : (w >> 10);
+    const uint32_t magic = static_cast<uint32_t>(25 - 2 * jj) << 10;
+    const uint32_t bits = (src & (0x00030003u << (2 * jj))) | (magic | (magic << 16));
+    __half2 h = *reinterpret_cast<const __half2*>(&bits);
+    h = __hmul2(__hsub2(h, cs[jj]), q2);
+    out[j] = *reinterpret_cast<const uint32_t*>(&h);
+  }
 }
 
 // Symmetric int8 code of one rotated value: clamp(rne(fl32(v inv)), -127, 127).

@@ -36,6 +36,7 @@ SIGNATURES = {
     "tl_prefill_workspace_size": (_I, [_I, _I, _I, _PSZ]),
     "tl_linear_prefill": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P, _SZ, _P]),
     "tl_linear_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P]),
+    "tl_linear_decode_tc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P]),
     "tl_linear_prefill_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P]),
     "tl_linear_decode_fused": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _P, _P, _P]),
     "tl_rotate_act": (_I, [_P, _I, _I, _P, _P, _P]),
@@ -203,6 +204,19 @@ def tl_linear_decode(packed, qT, sw, xq, sx, N: int, K: int, y_dtype: int = TL_B
     return y
 
 
+def tl_linear_decode_tc(packed, qT, sw, xq, sx, N: int, K: int, y_dtype: int = TL_BF16,
+                        y: torch.Tensor | None = None, acc_dbg: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
+    """Tensor-core decode for M <= 32; xq is the fp16 image of the codes [M,K]. Returns y [M,N]."""
+    _dev_tensor(xq, torch.float16, "xq")
+    M = xq.shape[0]
+    y = _linear_out(M, N, y_dtype, xq.device, y)
+    _check(lib().tl_linear_decode_tc(_ptr(packed), _ptr(qT), _ptr(sw), _ptr(xq), _ptr(sx), M, N, K,
+                                     _ptr(y), y_dtype, _ptr(acc_dbg), _stream(stream)),
+           "tl_linear_decode_tc")
+    return y
+
+
 def tl_linear_decode_fused(packed, qT, sw, x, N: int, K: int, y_dtype: int = TL_BF16,
                            signs=None, y: torch.Tensor | None = None,
                            acc_dbg: torch.Tensor | None = None, xq_out: torch.Tensor | None = None,
@@ -292,10 +306,25 @@ class TernaryLinear:
     kernel; both give the same integer accumulator and the same y.
     """
 
-    # The CUDA-core decode kernel wins while M * K is small; above, the tensor-core
-    # prefill does (measured on GB300 over M = 1..32: decode is faster up to
-    # M = 8 at K = 5120 and up to M = 4 at K = 17408).
+    # Which kernel serves a batch of M tokens (measured on GB300 over both MLP
+    # shapes, K = 5120 and 17408, 8 layer buffers in a CUDA graph): the dp4a
+    # CUDA-core decode up to 4 tokens; the mma.sync tensor-core decode for 5 to 8
+    # tokens, and up to 16 while K <= 8192 (M = 8: 16.6 against 19.9 us for dp4a;
+    # M = 16, K = 5120: 21.5 against 27.6 us for the prefill kernel); the tcgen05
+    # prefill kernel above.
+    DECODE_MAX_M = 4
     DECODE_MAX_MK = 72 * 1024
+    TC_MAX_M = 8
+    TC_MAX_M_SHALLOW = 16
+    TC_SHALLOW_K = 8192
+
+    def kernel_for(self, M: int) -> str:
+        """'decode', 'decode_tc' or 'prefill': the kernel forward() runs for M tokens."""
+        if M <= self.DECODE_MAX_M and M * self.K <= self.DECODE_MAX_MK:
+            return "decode"
+        if M <= self.TC_MAX_M or (M <= self.TC_MAX_M_SHALLOW and self.K <= self.TC_SHALLOW_K):
+            return "decode_tc"
+        return "prefill"
 
     def __init__(self, codes: torch.Tensor, s: torch.Tensor, device="cuda", y_dtype: int = TL_BF16):
         dev = torch.device(device)
@@ -322,10 +351,15 @@ class TernaryLinear:
         on_host = not x.is_cuda
         xd = x.to(self.device, non_blocking=True) if on_host else x
         M = xd.shape[0]
-        if M * self.K <= self.DECODE_MAX_MK:
+        kind = self.kernel_for(M)
+        if kind == "decode":
             xq, sx = tl_rotate_quant_act(xd, xq_dtype=TL_I8, stream=stream)
             y = tl_linear_decode(self.packed, self.qT, self.sw, xq, sx, self.N, self.K,
                                  self.y_dtype, y=out, stream=stream)
+        elif kind == "decode_tc":
+            xq, sx = tl_rotate_quant_act(xd, xq_dtype=TL_F16, stream=stream)
+            y = tl_linear_decode_tc(self.packed, self.qT, self.sw, xq, sx, self.N, self.K,
+                                    self.y_dtype, y=out, stream=stream)
         else:
             xq, sx = tl_rotate_quant_act(xd, xq_dtype=TL_F16, stream=stream)
             y = tl_linear_prefill(self.packed, self.qT, self.sw, xq, sx, self.N, self.K,
