@@ -257,6 +257,9 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="layer buffers per step (64 = the model's depth; fewer only for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--one", default=None, metavar="KERNEL:WORKLOAD:M",
+                    help="instead of the benchmark line: run one kernel (prefill, decode, decode_tc "
+                         "or picked) on one layer of a workload five times (for a profiler capture)")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-workload kernel times (down_proj M=256, the M-sweep subset)")
     ap.add_argument("--sweep", action="store_true",
@@ -269,6 +272,8 @@ def main(argv=None):
         return reference_main(args)
     if args.sweep:
         return sweep_main(args)
+    if args.one:
+        return one_main(args)
 
     import torch
 
@@ -690,6 +695,37 @@ def time_points(tl, synth, dev, stream, points, nl: int = 8, hbm_peak=None, tc_p
             raise RuntimeError(f"device status during {name} M={M}")
         out.append(line)
     return out
+
+
+def one_main(args) -> int:
+    """One kernel on one layer of a workload, five launches (for ncu captures)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from quantized_linear_layers_block_gb300 import synth, tl
+    kind, name, m = args.one.split(":")
+    M = int(m)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    codes, s_, x = synth.torch_config_layer(name, 0, M=M, device=str(dev))
+    lay = tl.TernaryLinear(codes, s_, device=dev)
+    N, K = lay.N, lay.K
+    if kind == "picked":
+        kind = lay.kernel_for(M)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    xq, sx = tl.tl_rotate_quant_act(x, xq_dtype=tl.TL_I8 if kind == "decode" else tl.TL_F16)
+    for _ in range(5):
+        if kind == "decode":
+            tl.tl_linear_decode(lay.packed, lay.qT, lay.sw, xq, sx, N, K, tl.TL_BF16, y=y)
+        elif kind == "decode_tc":
+            tl.tl_linear_decode_tc(lay.packed, lay.qT, lay.sw, xq, sx, N, K, tl.TL_BF16, y=y)
+        else:
+            tl.tl_linear_prefill(lay.packed, lay.qT, lay.sw, xq, sx, N, K, tl.TL_BF16, y=y,
+                                 workspace=lay._workspace(M))
+    torch.cuda.synchronize()
+    st = tl.tl_get_status()
+    print(json.dumps({"one": args.one, "kernel": kind, "M": M, "N": N, "K": K, "status": st}))
+    return 0 if st == tl.TL_OK else 1
 
 
 def sweep_main(args) -> int:
