@@ -162,6 +162,27 @@ def test_rotate_quant_bitexact(tl, name, xb, signs):
     assert np.array_equal(sx2.cpu().numpy(), sx.cpu().numpy())
 
 
+@pytest.mark.parametrize("K", [1024, 3072, 5120, 17408, 20480, 21504])
+@pytest.mark.parametrize("M", [1, 2, 3, 8])
+def test_rotate_quant_sizes(tl, M, K):
+    """K1 over odd and even token counts and block counts from 1 to 21, with and
+    without signs, both images, bit-exact."""
+    rng = np.random.default_rng(1000 * M + K // 1024)
+    xb = synth.activations_student_t(rng, M, K)
+    xq_ref, sx_ref = O.rotate_quant(xb)
+    signs = np.where(rng.random(K) < 0.5, -1, 1).astype(np.int8)
+    xq_s, sx_s = O.rotate_quant(xb, signs)
+    xd = dev(xb.view(np.int16), torch.bfloat16)
+    for sg, (xr, sr) in ((None, (xq_ref, sx_ref)), (dev(signs), (xq_s, sx_s))):
+        xq, sx = tl.tl_rotate_quant_act(xd, signs=sg, xq_dtype=tl.TL_I8)
+        xh, sx2 = tl.tl_rotate_quant_act(xd, signs=sg, xq_dtype=tl.TL_F16)
+        check_status(tl)
+        assert np.array_equal(xq.cpu().numpy(), xr)
+        assert np.array_equal(xh.cpu().numpy().astype(np.int64), xr.astype(np.int64))
+        assert np.array_equal(sx.cpu().numpy().view(np.uint32), sr.view(np.uint32))
+        assert np.array_equal(sx2.cpu().numpy().view(np.uint32), sr.view(np.uint32))
+
+
 def _tiny_tokens(K=2048):
     """Tokens of bf16 subnormals whose largest rotated value is below 127 / FLT_MAX,
     so that fl32(127 / a) overflows to +inf (the oracle's reading: non-zero
