@@ -33,7 +33,9 @@
 //                once per stage (on the A slot, whose expansion warps also saw
 //                the activations land), issues the stage's 16 MMAs and commits
 //                the A slot and the activation slot free: any other instruction
-//                in that thread costs tensor-pipe time, so it does nothing else.
+//                in that thread costs tensor-pipe time (it shares its SM
+//                sub-partition with busy warps), so the stage's MMAs are one
+//                block of straight-line code and it does nothing else.
 //   expansion    EPQ (2 or 4) warps per 32-lane quarter of tensor memory: lane
 //                = weight row; warp `part` turns its 256 / EPQ codes of the
 //                stage (q group part / (EPQ / 2)) into fp16 pairs in registers
@@ -218,6 +220,52 @@ __device__ __forceinline__ void drain_add(uint32_t taddr, int (&tot)[W]) {
   }
 }
 
+
+// The 16 MMAs of a stage: A columns a + 8 j, B boxes j / 4 (low descriptor
+// words b0..b3, high word bhi) at K steps j % 4 (32 bytes = 2 units each);
+// the first accumulates only if acc != 0.
+__device__ __forceinline__ void mma_stage16(uint32_t d, uint32_t a, uint32_t b0, uint32_t b1,
+                                            uint32_t b2, uint32_t b3, uint32_t bhi, uint32_t idesc,
+                                            uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p0, p1;\n .reg .b32 t;\n .reg .b64 bd;\n"
+      "setp.ne.b32 p0, %8, 0;\n setp.eq.b32 p1, %8, %8;\n"
+      "mov.b64 bd, {%2, %6};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %7, p0;\n"
+      "add.u32 t, %2, 2;\n mov.b64 bd, {t, %6};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+8], bd, %7, p1;\n"
+      "add.u32 t, %2, 4;\n mov.b64 bd, {t, %6};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+16], bd, %7, p1;\n"
+      "add.u32 t, %2, 6;\n mov.b64 bd, {t, %6};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+24], bd, %7, p1;\n"
+      "mov.b64 bd, {%3, %6};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+32], bd, %7, p1;\n"
+      "add.u32 t, %3, 2;\n mov.b64 bd, {t, %6};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+40], bd, %7, p1;\n"
+      "add.u32 t, %3, 4;\n mov.b64 bd, {t, %6};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+48], bd, %7, p1;\n"
+      "add.u32 t, %3, 6;\n mov.b64 bd, {t, %6};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+56], bd, %7, p1;\n"
+      "mov.b64 bd, {%4, %6};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+64], bd, %7, p1;\n"
+      "add.u32 t, %4, 2;\n mov.b64 bd, {t, %6};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+72], bd, %7, p1;\n"
+      "add.u32 t, %4, 4;\n mov.b64 bd, {t, %6};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+80], bd, %7, p1;\n"
+      "add.u32 t, %4, 6;\n mov.b64 bd, {t, %6};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+88], bd, %7, p1;\n"
+      "mov.b64 bd, {%5, %6};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+96], bd, %7, p1;\n"
+      "add.u32 t, %5, 2;\n mov.b64 bd, {t, %6};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+104], bd, %7, p1;\n"
+      "add.u32 t, %5, 4;\n mov.b64 bd, {t, %6};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+112], bd, %7, p1;\n"
+      "add.u32 t, %5, 6;\n mov.b64 bd, {t, %6};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+120], bd, %7, p1;\n"
+      "}" ::"r"(d), "r"(a), "r"(b0), "r"(b1), "r"(b2), "r"(b3), "r"(bhi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_p,
@@ -396,11 +444,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
             tc_fence_after();
             const uint64_t dslot = desc0 + static_cast<uint64_t>((b * C::B_BYTES) >> 4);
             const uint32_t aslot = tmem + A_COLS * a;
-#pragma unroll
-            for (int j = 0; j < MMAS_PER_STAGE; ++j) {
-              const uint32_t boff = (j >> 2) * (C::BOX_BYTES >> 4) + (j & 3) * (32 >> 4);
-              mma_f16_ts(d_addr, aslot + 8u * j, dslot + boff, C::IDESC, (st | j) != 0);
-            }
+            const uint32_t blo = static_cast<uint32_t>(dslot);
+            constexpr uint32_t BU = C::BOX_BYTES >> 4;
+            mma_stage16(d_addr, aslot, blo, blo + BU, blo + 2 * BU, blo + 3 * BU,
+                        static_cast<uint32_t>(dslot >> 32), C::IDESC, st != 0);
             tc_commit(aempty(a));
             tc_commit(bempty(b));
           }
