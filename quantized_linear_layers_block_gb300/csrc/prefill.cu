@@ -266,6 +266,15 @@ __device__ __forceinline__ void mma_stage16(uint32_t d, uint32_t a, uint32_t b0,
       : "memory");
 }
 
+// Two commits: both barriers see one arrival when the MMAs issued so far complete.
+__device__ __forceinline__ void tc_commit2(uint32_t bar1, uint32_t bar2) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];" ::"r"(bar1),
+      "r"(bar2)
+      : "memory");
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_p,
@@ -411,11 +420,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
     }
   } else if (warp == WARP_MMA) {
     if (lane == 0) {
-      uint32_t it = 0, cc = 0;
+      uint32_t cc = 0, aph = 0;
+      int a = 0, b = 0;   // A slot and activation slot of the next stage
       bool ok = true;
       // descriptor of activation slot 0, first box, first 16 columns: boxes are
       // BOX_BYTES apart, slots B_BYTES apart, and each 16-column step is 32 bytes
+      // (offsets that stay inside the descriptor's low word)
       const uint64_t desc0 = smem_desc_sw128(sbase + C::sb);
+      const uint32_t blo0 = static_cast<uint32_t>(desc0), bhi = static_cast<uint32_t>(desc0 >> 32);
+      constexpr uint32_t BU = C::BOX_BYTES >> 4, SU = C::B_BYTES >> 4;
       const int npieces = num_pieces(work, blockIdx.x);
       for (int k = 0; ok && k < npieces; ++k) {
         const Piece pc = get_piece(work, blockIdx.x, k);
@@ -430,10 +443,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
           }
           tc_fence_after();
           const uint32_t d_addr = tmem + C::D_COL0 + buf * BN;
-          for (int st = 0; st < STAGES_PER_CHUNK; ++st, ++it) {
-            const int b = it % NB;
-            const int a = it % NA;
-            const uint32_t aph = (it / NA) & 1u;
+#pragma unroll
+          for (int st = 0; st < STAGES_PER_CHUNK; ++st) {
             // one wait per 16 MMAs: the expansion warps arrive only after the
             // stage's activation tile has landed as well
             if (!mbar_wait(afull(a), aph, abort_flag)) {
@@ -442,14 +453,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
               break;
             }
             tc_fence_after();
-            const uint64_t dslot = desc0 + static_cast<uint64_t>((b * C::B_BYTES) >> 4);
-            const uint32_t aslot = tmem + A_COLS * a;
-            const uint32_t blo = static_cast<uint32_t>(dslot);
-            constexpr uint32_t BU = C::BOX_BYTES >> 4;
-            mma_stage16(d_addr, aslot, blo, blo + BU, blo + 2 * BU, blo + 3 * BU,
-                        static_cast<uint32_t>(dslot >> 32), C::IDESC, st != 0);
-            tc_commit(aempty(a));
-            tc_commit(bempty(b));
+            const uint32_t blo = blo0 + SU * b;
+            mma_stage16(d_addr, tmem + A_COLS * a, blo, blo + BU, blo + 2 * BU, blo + 3 * BU, bhi,
+                        C::IDESC, st != 0);
+            tc_commit2(aempty(a), bempty(b));
+            if (++a == NA) {
+              a = 0;
+              aph ^= 1u;
+            }
+            if (++b == NB) b = 0;
           }
           if (ok) tc_commit(dfull(buf));
         }
@@ -467,20 +479,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
     const int grp = part / (C::EPQ / 2);
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    uint32_t it = 0;
+    int w = 0, a = 0, b = 0;              // weight, A and activation slots of the stage
+    uint32_t wph = 0, aph = 0, bph = 0;   // and their phases
     bool ok = true;
     const int npieces = num_pieces(work, blockIdx.x);
     for (int k = 0; ok && k < npieces; ++k) {
       const Piece pc = get_piece(work, blockIdx.x, k);
       const int c0 = pc.c0, c1 = pc.c1;
       for (int c = c0; ok && c < c1; ++c) {
-        for (int st = 0; st < STAGES_PER_CHUNK; ++st, ++it) {
-          const int w = it % NW;
-          const uint32_t wph = (it / NW) & 1u;
-          const int a = it % NA;
-          const uint32_t aph = (it / NA) & 1u;
-          const int b = it % NB;
-          const uint32_t bph = (it / NB) & 1u;
+        for (int st = 0; st < STAGES_PER_CHUNK; ++st) {
           const bool got = mbar_wait(wfull(w), wph, abort_flag);
           if (!__all_sync(0xffffffffu, got)) {
             fail();
@@ -532,6 +539,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(afull(a));
+          if (++w == NW) {
+            w = 0;
+            wph ^= 1u;
+          }
+          if (++a == NA) {
+            a = 0;
+            aph ^= 1u;
+          }
+          if (++b == NB) {
+            b = 0;
+            bph ^= 1u;
+          }
         }
       }
     }
