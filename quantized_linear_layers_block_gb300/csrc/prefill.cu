@@ -25,7 +25,8 @@
 //   warp 0       weight producer: packed 2-bit codes of the 128 rows and their
 //                two q bytes per row and stage into a 4-deep ring (TMA); it
 //                starts before the kernel waits for the preceding one
-//                (programmatic dependent launch).
+//                (programmatic dependent launch). Like warps 1 and 2, the whole
+//                warp runs the loop and one elected lane issues.
 //   warp 2       activation producer: after that wait, the fp16 activation tile
 //                of the stage (four 128-byte-swizzled boxes of 64 columns) into a
 //                3-deep ring.
@@ -354,10 +355,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
     set_status(status, TL_ETIMEOUT);
   };
 
+  // The single-thread roles (the two TMA producers and the MMA issuer) run
+  // their loops on the whole warp with warp-uniform values; one elected lane
+  // issues the copies, MMAs and commits.
+  uint32_t elected;
+  asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}" : "=r"(elected));
   if (warp == WARP_WLOAD) {
-    if (lane == 0) {
-      tma_prefetch_desc(&map_p);
-      tma_prefetch_desc(&map_q);
+    {
+      if (elected) {
+        tma_prefetch_desc(&map_p);
+        tma_prefetch_desc(&map_q);
+      }
       uint32_t it = 0;
       bool ok = true;
       const int npieces = num_pieces(work, blockIdx.x);
@@ -368,15 +376,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
           for (int st = 0; st < STAGES_PER_CHUNK; ++st, ++it) {
             const int w = it % NW;
             const uint32_t ph = (it / NW) & 1u;
-            if (!mbar_wait(wempty(w), ph ^ 1u, abort_flag)) {
+            if (!__all_sync(0xffffffffu, mbar_wait(wempty(w), ph ^ 1u, abort_flag))) {
               fail();
               ok = false;
               break;
             }
             const int k0 = c * kBlock + st * BK;
-            mbar_arrive_expect_tx(wfull(w), W_TX);
-            tma_load_2d(sbase + C::sp + w * P_BYTES, &map_p, k0 / 4, nt * BM, wfull(w));
-            tma_load_2d(sbase + C::sq + w * Q_BYTES, &map_q, nt * BM, k0 / kGroup, wfull(w));
+            if (elected) {
+              mbar_arrive_expect_tx(wfull(w), W_TX);
+              tma_load_2d(sbase + C::sp + w * P_BYTES, &map_p, k0 / 4, nt * BM, wfull(w));
+              tma_load_2d(sbase + C::sq + w * Q_BYTES, &map_q, nt * BM, k0 / kGroup, wfull(w));
+            }
+            __syncwarp();
           }
         }
       }
@@ -387,8 +398,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
       }
     }
   } else if (warp == WARP_BLOAD) {
-    if (lane == 0) {
-      tma_prefetch_desc(&map_x);
+    {
+      if (elected) tma_prefetch_desc(&map_x);
       // the activations are written by the preceding kernel in the stream
       pdl_wait_prior();
       uint32_t it = 0;
@@ -401,31 +412,30 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
           for (int st = 0; st < STAGES_PER_CHUNK; ++st, ++it) {
             const int b = it % NB;
             const uint32_t ph = (it / NB) & 1u;
-            if (!mbar_wait(bempty(b), ph ^ 1u, abort_flag)) {
+            if (!__all_sync(0xffffffffu, mbar_wait(bempty(b), ph ^ 1u, abort_flag))) {
               fail();
               ok = false;
               break;
             }
             const int k0 = c * kBlock + st * BK;
-            mbar_arrive_expect_tx(bfull(b), C::B_BYTES);
+            if (elected) {
+              mbar_arrive_expect_tx(bfull(b), C::B_BYTES);
 #pragma unroll
-            for (int bx = 0; bx < BK / BOX_K; ++bx)
-              tma_load_2d(sbase + C::sb + b * C::B_BYTES + bx * C::BOX_BYTES, &map_x,
-                          k0 + bx * BOX_K, mt * BN, bfull(b));
+              for (int bx = 0; bx < BK / BOX_K; ++bx)
+                tma_load_2d(sbase + C::sb + b * C::B_BYTES + bx * C::BOX_BYTES, &map_x,
+                            k0 + bx * BOX_K, mt * BN, bfull(b));
+            }
+            __syncwarp();
           }
         }
       }
-      pdl_launch_dependents();
+      if (elected) pdl_launch_dependents();
       if (!ok) {
         const uint32_t n = it < NB ? it : NB;
         for (uint32_t i = it - n; i < it; ++i) mbar_wait(bfull(i % NB), (i / NB) & 1u, nullptr);
       }
     }
   } else if (warp == WARP_MMA) {
-    // the whole warp runs the loop (its values are warp-uniform); one elected
-    // lane issues the MMAs and commits
-    uint32_t elected;
-    asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}" : "=r"(elected));
     {
       uint32_t cc = 0, aph = 0;
       int a = 0, b = 0;   // A slot and activation slot of the next stage
@@ -661,9 +671,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
   }
 
   tc_fence_before();
-  // single-lane roles end at different times from the rest of their warp: the
-  // warp converges first so that the CTA barrier below waits for every thread
-  // (the tensor memory is released only after the last drain has read it)
+  // lanes of a warp can arrive here at different times (work done by one lane):
+  // the warp converges first so that the CTA barrier below waits for every
+  // thread (the tensor memory is released only after the last drain has read it)
   __syncwarp();
   __syncthreads();
   if (warp == WARP_MMA) {
