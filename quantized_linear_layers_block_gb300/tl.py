@@ -308,21 +308,21 @@ class TernaryLinear:
 
     # Which kernel serves a batch of M tokens (measured on GB300 over both MLP
     # shapes, K = 5120 and 17408, 8 layer buffers in a CUDA graph): the dp4a
-    # CUDA-core decode up to 4 tokens; the mma.sync tensor-core decode for 5 to 8
-    # tokens, and up to 16 while K <= 8192 (M = 8: 16.6 against 19.9 us for dp4a;
-    # M = 16, K = 5120: 21.5 against 27.6 us for the prefill kernel); the tcgen05
-    # prefill kernel above.
+    # CUDA-core decode up to 4 tokens; the mma.sync tensor-core decode for 5 to
+    # 12 tokens while K <= 8192 (M = 8: 16.6 against 20.0 us for dp4a and 20.9
+    # for the prefill kernel; M = 12: 20.8 against 21.2 us); the tcgen05 prefill
+    # kernel above, and from 5 tokens at deeper K (K = 17408, M = 5..8: 20.5
+    # against 24.1-24.4 us for the tensor-core decode).
     DECODE_MAX_M = 4
     DECODE_MAX_MK = 72 * 1024
-    TC_MAX_M = 8
-    TC_MAX_M_SHALLOW = 16
-    TC_SHALLOW_K = 8192
+    TC_MAX_M = 12
+    TC_MAX_K = 8192
 
     def kernel_for(self, M: int) -> str:
         """'decode', 'decode_tc' or 'prefill': the kernel forward() runs for M tokens."""
         if M <= self.DECODE_MAX_M and M * self.K <= self.DECODE_MAX_MK:
             return "decode"
-        if M <= self.TC_MAX_M or (M <= self.TC_MAX_M_SHALLOW and self.K <= self.TC_SHALLOW_K):
+        if M <= self.TC_MAX_M and self.K <= self.TC_MAX_K:
             return "decode_tc"
         return "prefill"
 
