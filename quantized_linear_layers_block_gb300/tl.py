@@ -309,13 +309,14 @@ class TernaryLinear:
     # Which kernel serves a batch of M tokens (measured on GB300 over both MLP
     # shapes, K = 5120 and 17408, 8 layer buffers in a CUDA graph): the dp4a
     # CUDA-core decode up to 4 tokens; the mma.sync tensor-core decode for 5 to
-    # 12 tokens while K <= 8192 (M = 8: 16.6 against 20.0 us for dp4a and 20.9
-    # for the prefill kernel; M = 12: 20.8 against 21.2 us); the tcgen05 prefill
-    # kernel above, and from 5 tokens at deeper K (K = 17408, M = 5..8: 20.5
-    # against 24.1-24.4 us for the tensor-core decode).
+    # 16 tokens while K <= 8192 (M = 8: 16.6 against 20.0 us for dp4a and 20.9
+    # for the prefill kernel; M = 16: the kernels tie at 21.5 us, the layer with
+    # its rotation takes 24.0 against 25.5 us); the tcgen05 prefill kernel above,
+    # and from 5 tokens at deeper K (K = 17408, M = 5..16: 20.5-20.8 against
+    # 24.1-32.8 us for the tensor-core decode).
     DECODE_MAX_M = 4
     DECODE_MAX_MK = 72 * 1024
-    TC_MAX_M = 12
+    TC_MAX_M = 16
     TC_MAX_K = 8192
 
     def kernel_for(self, M: int) -> str:
