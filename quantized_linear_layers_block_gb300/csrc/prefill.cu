@@ -32,10 +32,10 @@
 //                3-deep ring.
 //   warp 1       allocates tensor memory and issues the MMAs. The whole warp
 //                runs the loop on warp-uniform values and one elected lane
-//                issues: it waits once per stage (on the A slot, whose
-//                expansion warps also saw the activations land), issues the
-//                stage's 16 MMAs as one block of straight-line code and commits
-//                the A slot and the activation slot free. Every instruction on
+//                issues: per stage it waits for the activation tile and the
+//                A slot, issues the stage's 16 MMAs as one block of
+//                straight-line code and commits the A slot and the activation
+//                slot free. Every instruction on
 //                this path delays the tensor pipe (the warp shares its SM
 //                sub-partition with busy warps), so it does nothing else; the
 //                warp-uniform form measured 146 -> 135.5 us at the gate+up
@@ -44,8 +44,10 @@
 //                = weight row; warp `part` turns its 256 / EPQ codes of the
 //                stage (q group part / (EPQ / 2)) into fp16 pairs in registers
 //                and stores them into tensor memory as the MMA's A operand
-//                (tcgen05.st), then waits for the stage's activations and
-//                arrives on the A slot's full barrier.
+//                (tcgen05.st), then arrives on the A slot's full barrier (the
+//                activations are the MMA warp's wait: a wait taken out of the
+//                expansion warps' per-stage chain measured 133.8 -> 124.9 us
+//                at the gate+up shape with 512 tokens).
 //   drain        two warps per quarter (BN / 2 tokens each): after each
 //                1024-column chunk add the fp32 accumulator (double buffered)
 //                into int32 totals in registers; at the end of a tile write
@@ -73,6 +75,7 @@ constexpr int BOX_K = 64;           // columns per 128-byte swizzled activation 
 constexpr int STAGES_PER_CHUNK = kBlock / BK;
 constexpr int UMMA_K = 16;
 constexpr int MMAS_PER_STAGE = BK / UMMA_K;
+static_assert(MMAS_PER_STAGE == 16, "mma_stage16 issues one stage");
 constexpr int P_BYTES = BM * (BK / 4);        // 8 KB packed codes
 constexpr int Q_BYTES = BM * (BK / kGroup);   // 256 q bytes: [2 groups][128 rows]
 constexpr uint32_t W_TX = P_BYTES + Q_BYTES;
@@ -437,7 +440,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
     }
   } else if (warp == WARP_MMA) {
     {
-      uint32_t cc = 0, aph = 0;
+      uint32_t cc = 0, aph = 0, bph = 0;
       int a = 0, b = 0;   // A slot and activation slot of the next stage
       bool ok = true;
       const uint64_t desc0 = smem_desc_sw128(sbase + C::sb);
@@ -459,7 +462,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
           const uint32_t d_addr = tmem + C::D_COL0 + buf * BN;
 #pragma unroll
           for (int st = 0; st < STAGES_PER_CHUNK; ++st) {
-            if (!__all_sync(0xffffffffu, mbar_wait(afull(a), aph, abort_flag))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(bfull(b), bph, abort_flag) &&
+                                             mbar_wait(afull(a), aph, abort_flag))) {
               fail();
               ok = false;
               break;
@@ -476,7 +480,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
               a = 0;
               aph ^= 1u;
             }
-            if (++b == NB) b = 0;
+            if (++b == NB) {
+              b = 0;
+              bph ^= 1u;
+            }
           }
           if (ok && elected) tc_commit(dfull(buf));
           __syncwarp();
@@ -495,8 +502,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
     const int grp = part / (C::EPQ / 2);
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    int w = 0, a = 0, b = 0;              // weight, A and activation slots of the stage
-    uint32_t wph = 0, aph = 0, bph = 0;   // and their phases
+    int w = 0, a = 0;            // weight and A slots of the stage
+    uint32_t wph = 0, aph = 0;   // and their phases
     bool ok = true;
     const int npieces = num_pieces(work, blockIdx.x);
     for (int k = 0; ok && k < npieces; ++k) {
@@ -547,12 +554,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
           }
           tmem_wait_st();
           tc_fence_before();
-          const bool landed = mbar_wait(bfull(b), bph, abort_flag);
-          if (!__all_sync(0xffffffffu, landed)) {
-            fail();
-            ok = false;
-            break;
-          }
           __syncwarp();
           if (lane == 0) mbar_arrive(afull(a));
           if (++w == NW) {
@@ -562,10 +563,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
           if (++a == NA) {
             a = 0;
             aph ^= 1u;
-          }
-          if (++b == NB) {
-            b = 0;
-            bph ^= 1u;
           }
         }
       }
