@@ -77,6 +77,7 @@ constexpr int UMMA_K = 16;
 constexpr int MMAS_PER_STAGE = BK / UMMA_K;
 static_assert(MMAS_PER_STAGE == 16, "mma_stage16 issues one stage");
 constexpr int P_BYTES = BM * (BK / 4);        // 8 KB packed codes
+static_assert(BK / 4 == 64, "one 64-byte swizzle span of codes per weight row and stage");
 constexpr int Q_BYTES = BM * (BK / kGroup);   // 256 q bytes: [2 groups][128 rows]
 constexpr uint32_t W_TX = P_BYTES + Q_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
@@ -517,18 +518,26 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
             ok = false;
             break;
           }
-          const uint4* prow = reinterpret_cast<const uint4*>(smem + C::sp + w * P_BYTES +
-                                                             row * (BK / 4) + part * (C::EXP_WORDS * 4));
+          // the codes arrive 64-byte swizzled (TMA): 16-byte chunk c of row r sits
+          // at chunk c ^ ((r >> 1) & 3), so a quarter warp's eight rows hit all
+          // eight bank groups (unswizzled rows 64 bytes apart conflict 4-way)
+          const uint8_t* prow = smem + C::sp + w * P_BYTES + row * (BK / 4);
           uint4 pk[C::EXP_WORDS / 4];
 #pragma unroll
-          for (int i = 0; i < C::EXP_WORDS / 4; ++i) pk[i] = prow[i];
+          for (int i = 0; i < C::EXP_WORDS / 4; ++i) {
+            const int chunk = part * (C::EXP_WORDS / 4) + i;
+            pk[i] = *reinterpret_cast<const uint4*>(prow + ((chunk ^ ((row >> 1) & 3)) << 4));
+          }
           const int qv = static_cast<int8_t>(smem[C::sq + w * Q_BYTES + grp * BM + row]);
           // the slot is refilled by TMA (async proxy): order these ordinary
           // loads before the release, or the copy can overtake them
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(wempty(w));   // weight slot consumed
-          const __half qh = __int2half_rn(qv);
+          // q in [-127, 127] as fp16 without a conversion: 0x6400 + q + 128 is
+          // the fp16 of 1152 + q, exact; subtracting 1152 leaves q
+          const __half qh = __hsub(__ushort_as_half(static_cast<unsigned short>(0x6480 + qv)),
+                                   __ushort_as_half(0x6480));
           const __half2 q2 = __halves2half2(qh, qh);
           uint32_t out[32];
           expand_word(pk[0].x, q2, out + 0);
@@ -725,7 +734,7 @@ int launch_cfg(const PrefillArgs& a, int num_sms, int* status, cudaStream_t st, 
   if (!make_map_2d(enc, &mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.xq, a.K, a.M,
                    static_cast<uint64_t>(a.K) * 2, BOX_K, C::BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_2d(enc, &mp, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.packed, a.K / 4, a.N,
-                   static_cast<uint64_t>(a.K) / 4, BK / 4, BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                   static_cast<uint64_t>(a.K) / 4, BK / 4, BM, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map_2d(enc, &mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.qT, a.N, G, static_cast<uint64_t>(a.N),
                    BM, BK / kGroup, CU_TENSOR_MAP_SWIZZLE_NONE)) {
     return TL_EINVAL;
