@@ -25,8 +25,9 @@
 // slabs of gs groups into a ring of shared-memory buffers: the weights and q
 // by TMA tensor copies issued before the kernel waits for the preceding one
 // (programmatic dependent launch), each token's activations by a bulk copy
-// after. Eight consumer warps each own one row block and one part of every
-// slab's groups (kp = 8 / rbc parts).
+// after (lane m of the producer warp issues token m's). Eight consumer warps
+// each own one row block and one part of every slab's groups (kp = 8 / rbc
+// parts).
 #include "decode_common.cuh"
 
 #include <cuda_bf16.h>
@@ -129,37 +130,47 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
 
   if (warp == kTcConsumers) {
     // ------------------------------------------------------------- producer
-    if (lane == 0) {
-      tma_prefetch_desc(&map_w);
-      tma_prefetch_desc(&map_q);
+    // the whole warp runs the loop; one elected lane issues the weight copies
+    // and lane m issues token m's activation copy
+    uint32_t elected;
+    asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}" : "=r"(elected));
+    {
+      if (elected) {
+        tma_prefetch_desc(&map_w);
+        tma_prefetch_desc(&map_q);
+      }
       auto issue_w = [&](int s) {
         int g0;
         const int n = slab_groups(s, &g0);
         const int b = s % p.sb;
         const uint32_t buf = sbase + b * p.buf_bytes;
-        mbar_arrive_expect_tx(full(b), wbytes + qbytes + static_cast<uint32_t>(M) * n * 256);
-        tma_load_2d(buf, &map_w, g0 * 32, row0, full(b));
-        tma_load_2d(buf + p.off_q, &map_q, row0, g0, full(b));
+        if (elected) {
+          mbar_arrive_expect_tx(full(b), wbytes + qbytes + static_cast<uint32_t>(M) * n * 256);
+          tma_load_2d(buf, &map_w, g0 * 32, row0, full(b));
+          tma_load_2d(buf + p.off_q, &map_q, row0, g0, full(b));
+        }
+        __syncwarp();
       };
       auto issue_x = [&](int s) {
         int g0;
         const int n = slab_groups(s, &g0);
         const int b = s % p.sb;
         const uint32_t dst = sbase + b * p.buf_bytes + p.off_b;
-        for (int m = 0; m < M; ++m)
+        for (int m = lane; m < M; m += 32)
           bulk_g2s(dst + m * p.b_pitch, xq + static_cast<size_t>(m) * K + g0 * kGroup, n * 256,
                    full(b));
+        __syncwarp();
       };
       const int pre = nslab < p.sb ? nslab : p.sb;
       // weights and q only: they do not come from the preceding kernel
       for (int s = 0; s < pre; ++s) issue_w(s);
-      pdl_launch_dependents();
+      if (elected) pdl_launch_dependents();
       pdl_wait_prior();
       for (int s = 0; s < pre; ++s) issue_x(s);
       int issued = pre;
       for (int s = pre; s < nslab; ++s) {
         const int b = s % p.sb;
-        if (!mbar_wait(empty(b), static_cast<uint32_t>((s / p.sb) - 1) & 1u, abort_flag)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(empty(b), static_cast<uint32_t>((s / p.sb) - 1) & 1u, abort_flag))) {
           fail();
           break;
         }
@@ -211,8 +222,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                                   *reinterpret_cast<const uint32_t*>(wra + 16)};
           const uint32_t wb[2] = {*reinterpret_cast<const uint32_t*>(wrb),
                                   *reinterpret_cast<const uint32_t*>(wrb + 16)};
-          const __half qa = __int2half_rn(static_cast<int8_t>(buf[p.off_q + gg * rows + ra]));
-          const __half qb = __int2half_rn(static_cast<int8_t>(buf[p.off_q + gg * rows + rbw]));
+          // q in [-127, 127] as fp16 without a conversion: 0x6480 + q is the
+          // fp16 of 1152 + q (exact), minus 1152
+          const __half qa = __hsub(__ushort_as_half(static_cast<unsigned short>(
+                                       0x6480 + static_cast<int8_t>(buf[p.off_q + gg * rows + ra]))),
+                                   __ushort_as_half(0x6480));
+          const __half qb = __hsub(__ushort_as_half(static_cast<unsigned short>(
+                                       0x6480 + static_cast<int8_t>(buf[p.off_q + gg * rows + rbw]))),
+                                   __ushort_as_half(0x6480));
           const __half2 qa2 = __halves2half2(qa, qa), qb2 = __halves2half2(qb, qb);
           const uint8_t* bcol = buf + p.off_b + (gg * kGroup + 16 * t) * 2;
 #pragma unroll
