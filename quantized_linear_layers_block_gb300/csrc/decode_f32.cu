@@ -24,6 +24,9 @@
 // fused multiply-add adds code * xr exactly before its one rounding. The low
 // and high half words hold the even and odd codes of the same j, so one
 // packed fp32x2 add and one packed fp32x2 FMA per token handle two codes.
+// Each field is placed by one LOP3 with its mask as the immediate and the
+// magic in a register (with both as constants the compiler added a move per
+// LOP3: 12.4 M -> 9.7 M instructions, 17.4 -> 14.9 us at M = 1).
 #include "tl_internal.cuh"
 
 #include <cuda_bf16.h>
@@ -42,6 +45,26 @@ __device__ __forceinline__ uint64_t f2(float lo, float hi) {
 }
 __device__ __forceinline__ uint64_t f2_bits(uint32_t lo, uint32_t hi) {
   return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+// (x & (3 << 2 J)) | magic as one LOP3 with the mask as its immediate and the
+// magic in a register
+template <int J>
+__device__ __forceinline__ uint32_t field_or(uint32_t x, uint32_t magic) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(x), "n"(3u << (2 * J)), "r"(magic));
+  return d;
+}
+__device__ __forceinline__ uint32_t field_or_j(int j, uint32_t x, uint32_t magic) {
+  switch (j) {
+    case 0: return field_or<0>(x, magic);
+    case 1: return field_or<1>(x, magic);
+    case 2: return field_or<2>(x, magic);
+    case 3: return field_or<3>(x, magic);
+    case 4: return field_or<4>(x, magic);
+    case 5: return field_or<5>(x, magic);
+    case 6: return field_or<6>(x, magic);
+    default: return field_or<7>(x, magic);
+  }
 }
 __device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
 __device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
@@ -111,6 +134,8 @@ decode_f32_kernel(const uint2* __restrict__ packed, const __half* __restrict__ s
   }
   __syncthreads();
 
+  uint32_t magic_r;   // 1.5 * 2^23 (ulp 1), kept in a register for the LOP3s
+  asm volatile("mov.b32 %0, 0x4B400000;" : "=r"(magic_r));
   float acc[4][MT];
 #pragma unroll
   for (int r = 0; r < 4; ++r)
@@ -157,12 +182,10 @@ decode_f32_kernel(const uint2* __restrict__ packed, const __half* __restrict__ s
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int j = 2 * v + h;
-              const uint32_t magic = 0x4B400000u;                                 // 1.5 * 2^23: ulp 1
               const float neg = -(12582912.0f + static_cast<float>(1u << (2 * j)));   // -(1.5 * 2^23 + 4^j)
-              const uint32_t mask = 3u << (2 * j);
 #pragma unroll
               for (int r = 0; r < 4; ++r) {
-                uint64_t f = f2_bits((lo[r] & mask) | magic, (hi[r] & mask) | magic);
+                uint64_t f = f2_bits(field_or_j(j, lo[r], magic_r), field_or_j(j, hi[r], magic_r));
                 f = f2_add(f, f2(neg, neg));                                      // (even, odd) code * 4^j
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {

@@ -197,6 +197,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
 #pragma unroll
       for (int i = 0; i < 4; ++i) cf[0][j][i] = cf[1][j][i] = 0.f, acc[j][i] = 0;
     int ng = 0;                                          // groups summed in cf (both)
+    const ExpandMagic em = expand_magic();
     const uint32_t wpitch = static_cast<uint32_t>(p.gs) * 32;
     for (int s = 0; s < nslab; ++s) {
       const int b = s % p.sb;
@@ -236,8 +237,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
           for (int h = 0; h < 2; ++h) {
             // word t + 4h of the group: fp16 pairs (columns 16 (t + 4h) + 2e, + 1), e = 0..7
             uint32_t ea[8], eb[8];
-            expand_word(wa[h], qa2, ea);
-            expand_word(wb[h], qb2, eb);
+            expand_word(wa[h], qa2, ea, em);
+            expand_word(wb[h], qb2, eb, em);
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
               const int tok = 8 * j + g;                 // B column g of n-tile j

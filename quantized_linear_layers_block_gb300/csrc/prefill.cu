@@ -503,6 +503,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
     const int grp = part / (C::EPQ / 2);
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const ExpandMagic em = expand_magic();
     int w = 0, a = 0;            // weight and A slots of the stage
     uint32_t wph = 0, aph = 0;   // and their phases
     bool ok = true;
@@ -540,10 +541,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
                                    __ushort_as_half(0x6480));
           const __half2 q2 = __halves2half2(qh, qh);
           uint32_t out[32];
-          expand_word(pk[0].x, q2, out + 0);
-          expand_word(pk[0].y, q2, out + 8);
-          expand_word(pk[0].z, q2, out + 16);
-          expand_word(pk[0].w, q2, out + 24);
+          expand_word(pk[0].x, q2, out + 0, em);
+          expand_word(pk[0].y, q2, out + 8, em);
+          expand_word(pk[0].z, q2, out + 16, em);
+          expand_word(pk[0].w, q2, out + 24, em);
           // the A slot is free once the MMAs of the stage that used it last completed
           const bool free_slot = mbar_wait(aempty(a), aph ^ 1u, abort_flag);
           if (!__all_sync(0xffffffffu, free_slot)) {
@@ -555,10 +556,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
           const uint32_t aslot = lane_base + A_COLS * a + C::EXP_COLS * part;
           tmem_st_32x32b_x32(aslot, out);
           if constexpr (C::EXP_WORDS == 8) {
-            expand_word(pk[1].x, q2, out + 0);
-            expand_word(pk[1].y, q2, out + 8);
-            expand_word(pk[1].z, q2, out + 16);
-            expand_word(pk[1].w, q2, out + 24);
+            expand_word(pk[1].x, q2, out + 0, em);
+            expand_word(pk[1].y, q2, out + 8, em);
+            expand_word(pk[1].z, q2, out + 16, em);
+            expand_word(pk[1].w, q2, out + 24, em);
             tmem_st_32x32b_x32(aslot + 32, out);
           }
           tmem_wait_st();
