@@ -570,6 +570,11 @@ def main(argv=None):
                      "kernel": "prefill_kernel (K3)",
                      "timing": f"CUDA events around the prefill launch of every {EVENT_EVERY}th "
                                f"layer of the timed steps ({K * len(sampled)} launches)",
+                     # the kernel runs inside a long dense step (the power cap applies), hence
+                     # the sustained peak; the fraction of the burst peak beside it
+                     "timed_region_s": pre_ms * 1e-3,
+                     "frac_burst": k3_tops / float(peaks.get("bf16_tflops",
+                                                             FALLBACK_PEAKS["bf16_tflops"])),
                      "peak_source": f"{peak_src} bf16_tflops_sustained (the int8 GEMM runs on "
                                     "kind::f16 tensor cores; fp16 and bf16 share the rate)"},
         "decode": {
