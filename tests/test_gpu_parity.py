@@ -617,6 +617,26 @@ def test_argument_errors_launch_nothing(tl):
     check_status(tl)
 
 
+@pytest.mark.parametrize("K", [5120, 17408])
+@pytest.mark.parametrize("M", [1, 4, 5, 12, 16, 17, 40])
+def test_forward_every_route(tl, M, K):
+    """TernaryLinear.forward on each side of each kernel boundary (dp4a decode,
+    tensor-core decode, prefill) matches the oracle: bf16 y within one ulp of
+    the oracle's, f32 y identical."""
+    L = synth.config_inputs("decode", M=M, N=384, K=K)
+    lay = tl.TernaryLinear(torch.from_numpy(L.codes), torch.from_numpy(L.s))
+    lay32 = tl.TernaryLinear(torch.from_numpy(L.codes), torch.from_numpy(L.s), y_dtype=tl.TL_F32)
+    x = torch.from_numpy(L.x_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    y = lay.forward(x)
+    y32 = lay32.forward(x)
+    torch.cuda.synchronize()
+    check_status(tl)
+    r = O.layer(L.x_bits, L.codes, L.s)
+    yb = y.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.max(bf16_ulp_diff(yb, r["ybf"])) <= 1, lay.kernel_for(M)
+    assert np.array_equal(y32.cpu().numpy().view(np.uint32), r["y32"].view(np.uint32)), lay.kernel_for(M)
+
+
 def test_host_pipeline_matches_forward(tl):
     """tl.HostPipeline (copies overlapped with the kernels on three streams) gives the
     same bytes as TernaryLinear.forward on device tensors, for decode and prefill sizes."""
