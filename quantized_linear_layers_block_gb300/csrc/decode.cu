@@ -448,24 +448,39 @@ decodem_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ q
   }
 }
 
+// The four warps of rotating group g (named barrier 1 + g, 128 threads).
+__device__ __forceinline__ void group_sync(int g) {
+  if (g == 0)
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+  else
+    asm volatile("bar.sync 2, 128;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- M = 1, fused
 // One launch for the whole layer at M = 1: the kernel takes the bf16 token and
 // does the input-side rotation and the per-token quantisation itself (the
 // arithmetic of tl_rotate_quant_act, so the result is the same bit for bit)
-// before the M = 1 GEMV above (same rows per CTA, same register cap). The
-// grid runs in clusters of CS CTAs that share the token through distributed
-// shared memory: warp w of cluster rank r rotates block b = w CS + r, pushes
-// the block maximum to every CTA of the cluster, and after a cluster barrier
-// quantises its block, permutes it into the dp4a order (one chunk per lane)
-// and pushes the chunks and their sums to every CTA of the cluster; a second
-// barrier and the GEMV follows. So a token is rotated once per cluster, by
-// CTAs that would otherwise wait, and no CTA reads a peer after the second
-// barrier (each one's shared memory outlives every write into it). The
-// registers are capped for 4 CTAs per SM, not 5: under the 48-register cap
-// the rotation spills, and its local loads queue behind the weight stream
-// (10.2 us per layer against 8.0 at 64 registers). The rotation stays on the
-// critical path of every layer, so the two-launch rotate + GEMV pair remains
-// faster (7.2-7.4 us); clusters of 1, 2, 4 or 8 CTAs measured the same.
+// before the M = 1 GEMV above (same rows per CTA). The grid runs in clusters
+// of CS CTAs that share the token through distributed shared memory: in
+// cluster rank r, group g of four warps rotates block b = g CS + r (each lane
+// 8 elements: strides 1-4 in registers, 8-128 across lanes, 256 and 512
+// between the group's warps through shared memory), pushes the block maximum
+// to every CTA of the cluster, and after a cluster barrier quantises its
+// block, permutes it into the dp4a order (one chunk per lane of the group's
+// first warp) and pushes the chunks and their sums to every CTA of the
+// cluster; a second barrier and the GEMV follow. So a token is rotated once
+// per cluster, by CTAs that would otherwise wait, and no CTA reads a peer
+// after the second barrier (each one's shared memory outlives every write
+// into it). Registers are capped for 4 CTAs per SM, not 5: under the
+// 48-register cap the rotation spills. Per-CTA timestamps inside a 64-layer
+// graph put the pieces at: the wait on the preceding layer 0.5 us past its
+// last CTA, the token's load and rotation up to the first cluster barrier
+// 1.8 us, quantise + push up to the second 1.5 us, the GEMV 3-4 us; the
+// two-launch pair (rotate + quantise, then decode1_kernel) spends the same
+// ~3.6 us before its GEMV and stays slightly faster (7.2 against 8.2 us per
+// layer). One warp per block (5 of a cluster's warps) measured 8.3 us; every
+// CTA rotating the whole token itself (no cluster) 11.3 us, its 544 CTAs
+// reading the same 10 KB of activations.
 
 
 template <int PL, int CS>
@@ -475,23 +490,81 @@ decode1f_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ 
                 const int8_t* __restrict__ signs, int N, void* __restrict__ y, int y_dtype,
                 int32_t* __restrict__ acc_dbg, int8_t* __restrict__ xq_out,
                 float* __restrict__ sx_out) {
-  static_assert(PL <= kDecWarps * CS, "one rotating warp per block");
+  static_assert(PL <= 2 * CS, "two rotating groups of four warps per CTA");
   __shared__ __align__(16) M1Smem<PL> sm;
-  __shared__ __align__(16) int8_t xnat[kDecWarps][kBlock];   // a rotating warp's quantised block
+  __shared__ __align__(16) float xs[2][2][4][256];   // [group][stride 256 / 512][warp][element]
+  __shared__ __align__(16) int8_t xnat[2][kBlock];   // a group's quantised block, natural order
+  __shared__ float gmax[2][4];
   __shared__ float bmax[PL];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint2 ring[M1Traits<PL>::RC][M1Traits<PL>::RPW];
   m1_prologue<PL>(packed, qT, N, sm, ring);
   pdl_wait_prior();
 
+  // group g (warps 4 g .. 4 g + 3) of cluster rank r rotates block b = g CS + r;
+  // warp w4 of the group holds the elements 256 w4 + 8 lane + e
   const uint32_t rank = cluster_ctarank();
-  const int b = warp * CS + static_cast<int>(rank);     // the block this warp rotates, if b < PL
-  float v[4][8];
-  if (b < PL) {
-    float am = rotate_block_warp(x + b * kBlock, signs == nullptr ? nullptr : signs + b * kBlock, lane, v);
+  const int g = warp >> 2, w4 = warp & 3;
+  const int b = g * CS + static_cast<int>(rank);
+  const bool rot = b < PL;
+  const int i0 = 256 * w4 + 8 * lane;
+  float v[8];
+  if (rot) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(x + b * kBlock + i0);
+    const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(((wd[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << 16);
+    if (signs != nullptr) {
+      const uint2 sr = *reinterpret_cast<const uint2*>(signs + b * kBlock + i0);
+      const uint32_t sg[2] = {sr.x, sr.y};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int8_t sgn = static_cast<int8_t>((sg[e >> 2] >> (8 * (e & 3))) & 0xFFu);
+        if (sgn < 0) v[e] = -v[e];
+      }
+    }
+    // strides 1, 2, 4 (registers), 8 .. 128 (lanes), 256, 512 (the group's
+    // warps, through shared memory): the order and arithmetic of rotate_block_warp
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if ((e & h) == 0) fwht_bfly(v[e], v[e + h]);
+      }
+    }
+#pragma unroll
+    for (int t = 1; t < 32; t <<= 1) {
+      const float sg = (lane & t) != 0 ? -1.f : 1.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = __fmaf_rn(v[e], sg, __shfl_xor_sync(0xffffffffu, v[e], t));
+    }
+#pragma unroll
+    for (int st = 0; st < 2; ++st) {
+      float4* mine = reinterpret_cast<float4*>(&xs[g][st][w4][8 * lane]);
+      mine[0] = make_float4(v[0], v[1], v[2], v[3]);
+      mine[1] = make_float4(v[4], v[5], v[6], v[7]);
+      group_sync(g);
+      const float4* other = reinterpret_cast<const float4*>(&xs[g][st][w4 ^ (1 << st)][8 * lane]);
+      const float4 o0 = other[0], o1 = other[1];
+      const float o[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+      const bool upper = (w4 >> st) & 1;   // the upper warp of the pair keeps partner - own
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = upper ? __fsub_rn(o[e], v[e]) : __fadd_rn(v[e], o[e]);
+    }
+    float am = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      v[e] = __fmul_rn(v[e], 0.03125f);
+      am = fmaxf(am, fabsf(v[e]));
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-    if (lane < CS) st_peer(peer_addr(&bmax[b], lane), am);
+    if (lane == 0) gmax[g][w4] = am;
+    group_sync(g);
+    if (w4 == 0 && lane < CS) {
+      const float bm = fmaxf(fmaxf(gmax[g][0], gmax[g][1]), fmaxf(gmax[g][2], gmax[g][3]));
+      st_peer(peer_addr(&bmax[b], lane), bm);
+    }
   }
   cluster_sync();
   float a = 0.f;
@@ -499,29 +572,30 @@ decode1f_kernel(const uint32_t* __restrict__ packed, const int8_t* __restrict__ 
   for (int i = 0; i < PL; ++i) a = fmaxf(a, bmax[i]);
   const float inv = a > 0.f ? __fdiv_rn(127.f, a) : 0.f;
   const float sx0 = a > 0.f ? __fdiv_rn(a, 127.f) : 0.f;
-  if (b < PL) {
-    const bool out = xq_out != nullptr && blockIdx.x < CS;   // the first cluster writes xq_out
+  if (rot) {
+    int q8[8];
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      int q8[8];
+    for (int e = 0; e < 8; ++e) q8[e] = quant_i8(v[e], inv);
+    uint2 o;
+    o.x = (q8[0] & 0xFF) | ((q8[1] & 0xFF) << 8) | ((q8[2] & 0xFF) << 16) | ((q8[3] & 0xFF) << 24);
+    o.y = (q8[4] & 0xFF) | ((q8[5] & 0xFF) << 8) | ((q8[6] & 0xFF) << 16) | ((q8[7] & 0xFF) << 24);
+    *reinterpret_cast<uint2*>(&xnat[g][i0]) = o;
+    if (xq_out != nullptr && blockIdx.x < CS)   // the first cluster writes xq_out
+      *reinterpret_cast<uint2*>(xq_out + b * kBlock + i0) = o;
+    group_sync(g);
+    if (w4 == 0) {
+      // lane c permutes chunk c of the block into the dp4a order and pushes it
+      // with its sum to every CTA of the cluster
+      const uint4* src = reinterpret_cast<const uint4*>(&xnat[g][32 * lane]);
+      uint4 p0, p1;
+      const int cs = permute_chunk(src[0], src[1], p0, p1);
+      const int c = b * 32 + lane;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) q8[e] = quant_i8(v[jj][e], inv);
-      uint2 o;
-      o.x = (q8[0] & 0xFF) | ((q8[1] & 0xFF) << 8) | ((q8[2] & 0xFF) << 16) | ((q8[3] & 0xFF) << 24);
-      o.y = (q8[4] & 0xFF) | ((q8[5] & 0xFF) << 8) | ((q8[6] & 0xFF) << 16) | ((q8[7] & 0xFF) << 24);
-      *reinterpret_cast<uint2*>(&xnat[warp][256 * jj + 8 * lane]) = o;
-      if (out) *reinterpret_cast<uint2*>(xq_out + b * kBlock + 256 * jj + 8 * lane) = o;
-    }
-    __syncwarp();
-    const uint4* src = reinterpret_cast<const uint4*>(&xnat[warp][32 * lane]);
-    uint4 p0, p1;
-    const int cs = permute_chunk(src[0], src[1], p0, p1);
-    const int c = b * 32 + lane;                          // chunk of the token
-#pragma unroll
-    for (int r = 0; r < CS; ++r) {
-      st_peer(peer_addr(&sm.xw0[c], r), p0);
-      st_peer(peer_addr(&sm.xw1[c], r), p1);
-      st_peer(peer_addr(&sm.csum[c], r), cs);
+      for (int r = 0; r < CS; ++r) {
+        st_peer(peer_addr(&sm.xw0[c], r), p0);
+        st_peer(peer_addr(&sm.xw1[c], r), p1);
+        st_peer(peer_addr(&sm.csum[c], r), cs);
+      }
     }
   }
   if (sx_out != nullptr && blockIdx.x == 0 && tid == 0) sx_out[0] = sx0;
