@@ -127,13 +127,16 @@ int tl_rotate_quant_act(const uint16_t* x, int M, int K, const int8_t* signs,
 
 /*
  * Workspace bytes that let tl_linear_prefill split the K dimension across
- * CTAs: the output tiles that do not fill a whole round of SMs (all of them
- * when there are fewer tiles than SMs) are cut into equal ranges of
- * 1024-column chunks, one per CTA, and a cut tile's partial int32 sums meet in
- * a slot of the workspace (512 bytes per token of the tile: 64 KB for a
- * 128-token tile, 8 KB for the 16-token tiles of a batch of at most 16
- * tokens; plus 4 bytes per slot). With a smaller (or NULL) workspace the call
- * still succeeds, unsplit.
+ * CTAs (0 when it would not: then every output tile runs whole on one CTA).
+ * A problem is split when whole tiles would leave the busiest SM more than
+ * six 1024-column chunks above an even share (few tiles with a long K): the
+ * tiles of the last partial round of SMs (all of them when there are fewer
+ * tiles than SMs) are cut into equal chunk ranges over at most four CTAs per
+ * tile, and a cut tile's partial int32 sums meet in a slot of the workspace:
+ * one region of 512 bytes per token of the tile for each CTA that may share
+ * it (64 KB for a 128-token tile, 8 KB for the 16-token tiles of a batch of
+ * at most 16 tokens), plus 32 bytes of counters. With a smaller (or NULL)
+ * workspace the call still succeeds, unsplit.
  */
 int tl_prefill_workspace_size(int M, int N, int K, size_t* bytes);
 
@@ -230,9 +233,9 @@ int tl_linear_decode_fused(const uint8_t* packed, const int8_t* qT, const float*
 
 /*
  * Bytes of the library-owned scratch array used by tl_linear_prefill_noalloc
- * (8 MiB, held on every device that loads the library until the process exits).
+ * (16 MiB, held on every device that loads the library until the process exits).
  */
-#define TL_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+#define TL_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 
 /*
  * tl_linear_prefill without a caller workspace, for callers that cannot
@@ -248,16 +251,15 @@ int tl_linear_decode_fused(const uint8_t* packed, const int8_t* qT, const float*
  * by the library; the call clears the part it uses before the kernel (so a
  * call that gave up earlier leaves nothing behind for the next). If that
  * part would exceed the array (see tl_prefill_workspace_size) the call returns
- * TL_ENOSPACE and launches nothing. With at least as many tiles as SMs only
- * the last partial round is split; if that does not fit either, every tile
- * runs whole (same result). The call allocates nothing and calls no
- * allocating routine.
+ * TL_ENOSPACE and launches nothing, when there are fewer tiles than SMs; with
+ * more, a split that does not fit runs every tile whole instead (same
+ * result). The call allocates nothing and calls no allocating routine.
  *
  * - Every call shares the one array per device: calls that can overlap on the
  *   GPU (other streams, other host threads) race on it; serialise them.
  * - The first call on a device looks up the array's device address, and the
  *   first prefill call of either entry point on a device loads the library's
- *   kernels together with the array, which reserves its 8 MiB of device memory
+ *   kernels together with the array, which reserves its 16 MiB of device memory
  *   and may synchronise the device. Make one call during set-up, before any
  *   stream capture and before the device memory is handed out.
  * - The library caches that address (and its status word's) per device: do not

@@ -54,10 +54,12 @@
 //                y = (fl32(acc) sw[n]) sx[m].
 // Tensor memory (512 columns x 128 lanes): NA A slots of 128 columns from
 // column 0, then two fp32 accumulators of BN columns.
-// When the problem has fewer tiles than SMs, K is split across CTAs; partial
-// int32 sums meet in a caller workspace and the last CTA of a tile finishes it
-// and returns the tile's part of the workspace to zero, so the workspace needs
-// zeroing only once, when it is allocated.
+// When whole tiles would load the SMs unevenly (few tiles with a long K), the
+// tiles of the last partial round are cut along K across CTAs; each piece
+// stores its partial int32 sums in its own region of a caller workspace and
+// the last CTA of a tile to arrive adds the others' regions, finishes it and
+// returns the regions to zero, so the workspace needs zeroing only once, when
+// it is allocated.
 #include "tl_internal.cuh"
 
 #include <cuda_bf16.h>
@@ -104,8 +106,8 @@ struct Cfg {
   static constexpr int sp = sb + NB * B_BYTES;
   static constexpr int sq = sp + NW * P_BYTES;
   static constexpr int sbar = sq + NW * Q_BYTES;
-  // wfull[NW] wempty[NW] bfull[NB] bempty[NB] afull[NA] aempty[NA] dfull[2] dempty[2] fin rdv1 rdv2
-  static constexpr int n_bars = 2 * NW + 2 * NB + 2 * NA + 2 + 2 + 3;
+  // wfull[NW] wempty[NW] bfull[NB] bempty[NB] afull[NA] aempty[NA] dfull[2] dempty[2] fin
+  static constexpr int n_bars = 2 * NW + 2 * NB + 2 * NA + 2 + 2 + 1;
   static constexpr int smisc = sbar + n_bars * 8;
   static constexpr int stotal = smisc + 16;
   static_assert(stotal + 1024 <= 232448, "shared memory budget");
@@ -122,20 +124,25 @@ using Cfg32 = Cfg<32, 12, 4, 3, 4>;
 using Cfg16 = Cfg<16, 16, 4, 3, 4>;
 
 // Work schedule. Tiles [0, full) are whole units, dealt round-robin to the
-// grid (full is a multiple of the grid, so every CTA gets the same number).
-// The remaining `tail` tiles form a chunk space of tail * chunks chunks that is
-// cut into `tgrid` contiguous, equal ranges, one per CTA 0 .. tgrid-1 (each at
-// least one chunk): a CTA's range covers pieces of one or more tiles. A tile
-// cut between CTAs meets in workspace slot (tile - full): every piece adds its
-// int32 partial sums there and the last of the tile's contributors writes it.
+// grid (all of them unless plan_work finds the imbalance worth a cut). The
+// remaining `tail` tiles form a chunk space of tail * chunks chunks that is
+// cut into `tgrid` contiguous, equal ranges, one per CTA 0 .. tgrid-1 (each
+// at least one chunk): a CTA's range covers pieces of one or more tiles. A
+// tile cut between CTAs meets in workspace slot (tile - full), through nreg
+// regions: with few CTAs per tile (nreg = their most) every piece stores its
+// int32 partial sums in its own region (contributor ci); with more (nreg = 1)
+// every piece adds them into the one region with atomics. Per drain warp a
+// counter tells the last of the tile's contributors to arrive, which gathers
+// the sums and writes the tile.
 struct Work {
-  int mtiles, chunks, full, tail, tgrid;
+  int mtiles, chunks, full, tail, tgrid, nreg;
 };
 
 struct Piece {
   int nt, mt, c0, c1;   // tile (weight-row block, token block) and chunk range
   int slot;             // workspace slot, or -1 for a whole tile
   int contrib;          // CTAs that share the tile (1 for a whole tile)
+  int ci;               // this CTA's place among them
 };
 
 __device__ __forceinline__ int num_pieces(const Work& w, int b) {
@@ -160,6 +167,7 @@ __device__ __forceinline__ Piece get_piece(const Work& w, int b, int k) {
     p.c1 = w.chunks;
     p.slot = -1;
     p.contrib = 1;
+    p.ci = 0;
   } else {
     const int T = w.tail * w.chunks;
     const int s = b * T / w.tgrid, e = (b + 1) * T / w.tgrid;
@@ -171,6 +179,7 @@ __device__ __forceinline__ Piece get_piece(const Work& w, int b, int k) {
     const int first = ((lo + 1) * w.tgrid - 1) / T;
     const int last = (hi * w.tgrid - 1) / T;
     p.contrib = last - first + 1;
+    p.ci = b - first;
     p.slot = p.contrib > 1 ? tt : -1;
     tile = w.full + tt;
   }
@@ -310,11 +319,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
   auto dfull = [&](int i) { return bar0 + 8u * (2 * NW + 2 * NB + 2 * NA + i); };
   auto dempty = [&](int i) { return bar0 + 8u * (2 * NW + 2 * NB + 2 * NA + 2 + i); };
   const uint32_t fin = bar0 + 8u * (2 * NW + 2 * NB + 2 * NA + 4);
-  const uint32_t rdv1 = fin + 8u;
-  const uint32_t rdv2 = fin + 16u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::smisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::smisc + 4);
-  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::smisc + 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -339,10 +345,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
       mbar_init(dempty(i), N_DRAIN_WARPS);
     }
     mbar_init(fin, 1);
-    mbar_init(rdv1, N_DRAIN_WARPS);
-    mbar_init(rdv2, 1);
     *abort_flag = 0;
-    *last_flag = 0;
     fence_barrier_init();
   }
   if (warp == WARP_MMA) {
@@ -582,7 +585,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
     const int half = (warp - WARP_DRAIN0) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    uint32_t cc = 0, ku = 0;
+    uint32_t cc = 0;
     bool ok = true;
     const int npieces = num_pieces(work, blockIdx.x);
     for (int k = 0; ok && k < npieces; ++k) {
@@ -610,57 +613,55 @@ prefill_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
       const int n = nt * BM + row;
       const int mbase = mt * BN + half * HB;
       bool finish = ok;
-      if (slot >= 0) {
-        // Rendezvous of the drain warps through two mbarriers (bounded waits):
-        // every warp adds its partial sums into the tile's workspace slot
-        // ([token][row] within the tile), the leader counts the tile's finished
-        // splits, and the CTA that completes the tile writes it and returns the
-        // slot and its count to zero for the next call.
-        int32_t* wsl = ws_acc + static_cast<size_t>(slot) * (BM * BN) + (half * HB) * BM + row;
-        const uint32_t rp = ku & 1u;
-        ++ku;
-        if (ok) {
+      if (slot >= 0 && ok) {
+        // the warp's slice of the tile ([token][row] within a region): with one
+        // region per contributor it stores its sums in its own (plain stores),
+        // else it adds them into the single region; the warp's counter for the
+        // tile then says whether every other contributor's same warp is done.
+        // The last one gathers the sums, writes the tile and returns the
+        // regions and the counter to zero for the next call.
+        const size_t region = static_cast<size_t>(BM) * BN;
+        int32_t* ws_tile = ws_acc + static_cast<size_t>(slot) * work.nreg * region + (half * HB) * BM + row;
+        const bool own_regions = work.nreg > 1;
+        int32_t* dst = ws_tile + (own_regions ? static_cast<size_t>(pc.ci) * region : 0);
 #pragma unroll
-          for (int j = 0; j < HB; ++j) {
-            const int m = mbase + j;
-            if (m < M) atomicAdd(wsl + j * BM, tot[j]);
-          }
-          __threadfence();
+        for (int j = 0; j < HB; ++j) {
+          if (own_regions)
+            __stcg(dst + j * BM, tot[j]);
+          else
+            atomicAdd(dst + j * BM, tot[j]);
         }
+        __threadfence();
         __syncwarp();
-        if (lane == 0) mbar_arrive(rdv1);
-        if (warp == WARP_DRAIN0 && lane == 0) {
-          int last = 0;
-          if (mbar_wait(rdv1, rp, abort_flag)) {
-            if (!*abort_flag) {
-              __threadfence();
-              last = atomicAdd(ws_cnt + slot, 1) == pc.contrib - 1;
-              // every contributor has counted itself: nothing reads the count again
-              if (last) ws_cnt[slot] = 0;
-            }
-          } else {
-            fail();
-          }
-          *last_flag = last;
-          mbar_arrive(rdv2);
+        int* cnt = ws_cnt + slot * N_DRAIN_WARPS + (warp - WARP_DRAIN0);
+        int last = 0;
+        if (lane == 0) {
+          last = atomicAdd(cnt, 1) == pc.contrib - 1;
+          // every contributor has counted itself: nothing reads the count again
+          if (last) *cnt = 0;
         }
-        const bool got = mbar_wait(rdv2, rp, abort_flag);
-        if (!__all_sync(0xffffffffu, got)) {
-          fail();
-          ok = false;
-        }
-        finish = ok && *last_flag != 0;
+        finish = __shfl_sync(0xffffffffu, last, 0) != 0;
         if (finish) {
           __threadfence();
+          // own regions: add the others' (this CTA's sums are in tot already);
+          // one shared region: it holds every piece's sums
+          const int nparts = own_regions ? pc.contrib : 1;
+#pragma unroll 1
+          for (int c = 0; c < nparts; ++c) {
+            int32_t* part = ws_tile + static_cast<size_t>(c) * region;
+            const bool mine = own_regions && c == pc.ci;
 #pragma unroll
-          for (int j = 0; j < HB; ++j) {
-            const int m = mbase + j;
-            if (m < M) {
-              tot[j] = __ldcg(wsl + j * BM);
-              __stcg(wsl + j * BM, 0);
+            for (int j = 0; j < HB; ++j) {
+              if (!mine) {
+                const int v = __ldcg(part + j * BM);
+                tot[j] = own_regions ? tot[j] + v : v;
+              }
+              __stcg(part + j * BM, 0);
             }
           }
         }
+      } else if (slot >= 0) {
+        finish = false;
       }
       if (finish) {
         const float swn = sw[n];
@@ -701,26 +702,48 @@ size_t plan_work(int M, int N, int K, int num_sms, Work* w, int* grid) {
   const int bn = tile_tokens(M);
   w->mtiles = (M + bn - 1) / bn;
   w->chunks = K / kBlock;
+  w->nreg = 1;
   const int tiles = w->mtiles * (N / BM);
-  if (tiles >= num_sms) {
-    *grid = num_sms;
-    w->full = tiles / num_sms * num_sms;
-  } else {
-    const int total = tiles * w->chunks;
-    *grid = total < num_sms ? total : num_sms;
-    w->full = 0;
-  }
-  w->tail = tiles - w->full;
-  const int T = w->tail * w->chunks;
-  w->tgrid = T < *grid ? T : *grid;
-  if (w->tail == 0 || w->tgrid == w->tail) {
-    // nothing is cut: every tail tile is one CTA's whole range
+  // whole tiles dealt round-robin, unless that leaves the busiest CTA more
+  // than kSplitGain chunks above an even share: the meeting of a cut tile's
+  // partial sums costs about that much (measured 14-18 us, 5-6 chunks), so a
+  // smaller imbalance is cheaper to keep (17408 x 5120 with 256 tokens, 1.79
+  // tiles per SM: 35.2 us whole against 41.0 cut; with 64 tokens, 0.89 tiles
+  // per SM: 17.0 against 22.5; down_proj with 256 tokens, 80 tiles of 17
+  // chunks: 41.7 cut against 52.7 whole)
+  constexpr int kSplitGain = 6;
+  *grid = tiles < num_sms ? tiles : num_sms;
+  const int busiest = (tiles + num_sms - 1) / num_sms * w->chunks;
+  const bool cut = static_cast<long long>(busiest) * num_sms - static_cast<long long>(tiles) * w->chunks >
+                   static_cast<long long>(kSplitGain) * num_sms;
+  if (!cut) {
     w->full = tiles;
     w->tail = 0;
     w->tgrid = 0;
     return 0;
   }
-  return static_cast<size_t>(w->tail) * (BM * bn) * 4 + static_cast<size_t>(w->tail) * 4;
+  // the tiles of the last partial round (all of them when there are fewer
+  // tiles than SMs) are cut into equal chunk ranges over the CTAs; a tile
+  // shared by at most three CTAs meets through one region per CTA (the
+  // finishing CTA adds up to two regions), one shared by more through
+  // atomics into one region (down_proj with 256 tokens, 80 tiles cut over 152
+  // CTAs: 41.7 us through regions against 51.1 through atomics; 5120 x 17408
+  // with 1024 tokens, 16 tiles cut over 152 CTAs: 116 us through atomics,
+  // 132 through regions)
+  *grid = num_sms;
+  w->full = tiles / num_sms * num_sms;
+  w->tail = tiles - w->full;
+  const int T = w->tail * w->chunks;
+  w->tgrid = T < num_sms ? T : num_sms;
+  int maxc = 1;
+  for (int tt = 0; tt < w->tail; ++tt) {   // the CTAs that share each tile (as get_piece)
+    const int lo = tt * w->chunks, hi = lo + w->chunks;
+    const int first = ((lo + 1) * w->tgrid - 1) / T, last = (hi * w->tgrid - 1) / T;
+    if (last - first + 1 > maxc) maxc = last - first + 1;
+  }
+  w->nreg = maxc <= 3 ? maxc : 1;
+  return static_cast<size_t>(w->tail) * w->nreg * (BM * bn) * 4 +
+         static_cast<size_t>(w->tail) * N_DRAIN_WARPS * 4;
 }
 
 template <class C>
@@ -752,13 +775,14 @@ int launch_cfg(const PrefillArgs& a, int num_sms, int* status, cudaStream_t st, 
       w.full = w.mtiles * (a.N / BM);
       w.tail = 0;
       w.tgrid = 0;
+      w.nreg = 1;
       if (grid > w.full) grid = w.full;
     } else {
       // the workspace is zero (zeroed by the caller once, and returned to zero
       // by every call that completes); the no-alloc entry clears it anyway
       ws_acc = static_cast<int32_t*>(a.workspace);
       ws_cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(a.workspace) +
-                                      static_cast<size_t>(w.tail) * (BM * C::BN) * 4);
+                                      static_cast<size_t>(w.tail) * w.nreg * (BM * C::BN) * 4);
       if (a.clear_workspace &&
           (*cerr = cudaMemsetAsync(a.workspace, 0, need, st)) != cudaSuccess)
         return TL_ECUDA;

@@ -165,8 +165,7 @@ int tl_linear_prefill_noalloc(const uint8_t* packed, const int8_t* qT, const flo
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return TL_ECUDA;
   // with fewer tiles than SMs the split is the point: refuse what does not fit;
-  // otherwise only the last partial round would be split, and without room the
-  // kernel runs every tile whole
+  // with more, a split without room runs every tile whole
   if (need > tl::kNoAllocScratchBytes && tl::prefill_split_required(M, N, sms)) return TL_ENOSPACE;
   int* status = nullptr;
   if ((r = status_ptr(&status)) != TL_OK) return r;

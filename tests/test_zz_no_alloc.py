@@ -22,6 +22,8 @@ pytestmark = pytest.mark.gpu
 
 FP32_TOL = 1e-3
 
+LIMIT = 16 * 1024 * 1024   # TL_NOALLOC_SCRATCH_BYTES
+
 
 @pytest.fixture(scope="module")
 def tl():
@@ -41,7 +43,7 @@ def test_noalloc_matches_workspace_version_on_two_calls(tl):
     # few output tiles and a long K: the kernel splits K and uses the scratch
     L = synth.config_inputs("down_proj", M=64, N=256, K=17408)
     need = tl.tl_prefill_workspace_size(L.M, L.N, L.K)
-    assert 0 < need <= 8 * 1024 * 1024
+    assert 0 < need <= LIMIT
     packed, qT, sw = tl.tl_pack_weights(_dev(L.codes), _dev(L.s.view(np.int16), torch.float16))
     x = _dev(L.x_bits.view(np.int16), torch.bfloat16)
     xq, sx = tl.tl_rotate_quant_act(x, xq_dtype=tl.TL_F16)
@@ -60,8 +62,7 @@ def test_noalloc_matches_workspace_version_on_two_calls(tl):
         assert err <= FP32_TOL
 
 
-LIMIT = 8 * 1024 * 1024
-M_TILE = 128      # a 128-token batch runs on one 128-token tile; its split-K slot is 64 KB
+M_TILE = 128      # a 128-token batch runs on one 128-token tile: 64 KB per split-K region
 
 
 def _sms():
@@ -107,15 +108,19 @@ def test_noalloc_allocates_nothing(tl):
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch(tl):
-    """Fewer tiles than SMs (K must be split) and more split-K scratch than the
-    array holds: refused before any launch."""
+    """Fewer tiles than SMs with a long K (K is cut) and more split-K scratch
+    than the array holds: refused before any launch."""
     sms = _sms()
-    M, K = M_TILE, 2048
-    # the most 128-row tiles below the SM count: all of them are cut along K
-    N = (sms - 1) * 128
-    need = tl.tl_prefill_workspace_size(M, N, K)
-    if need <= LIMIT:
+    M, K = M_TILE, 32768
+    shape = None
+    for tiles in range(sms - 1, 0, -1):   # 128-row tiles of one 128-token block
+        need = tl.tl_prefill_workspace_size(M, tiles * 128, K)
+        if need > LIMIT:
+            shape = tiles * 128
+            break
+    if shape is None:
         pytest.skip(f"with {sms} SMs no single-tile-row problem needs more than the array holds")
+    N = shape
     assert (N // 128) < sms
     packed, qT, sw, xq, sx = _zeros_layer(M, N, K)
     y = torch.full((M, N), 7.0, dtype=torch.float32, device="cuda")
@@ -125,20 +130,19 @@ def test_noalloc_refuses_problems_beyond_its_scratch(tl):
 
 
 def test_noalloc_runs_unsplit_when_tiles_fill_the_gpu(tl):
-    """At least as many tiles as SMs: only the last partial round would be split;
-    when its scratch does not fit, every tile runs whole and the result is the
-    same as tl_linear_prefill's."""
+    """At least as many tiles as SMs, with a short K: whole tiles even though
+    the last round fills only part of the GPU; no scratch is needed, and the
+    result is the same as tl_linear_prefill's."""
     sms = _sms()
     M, K = M_TILE, 2048
-    N = (sms + 140) * 128          # one full round, then 140 tiles left over (> 128 slots of 64 KB)
+    N = (sms + 140) * 128          # one full round, then 140 tiles left over
     need = tl.tl_prefill_workspace_size(M, N, K)
-    assert (N // 128) >= sms and need > LIMIT
+    assert (N // 128) >= sms and need == 0
     L = synth.config_inputs("gate_up", M=M, N=N, K=K)
     packed, qT, sw = tl.tl_pack_weights(_dev(L.codes), _dev(L.s.view(np.int16), torch.float16))
     xq, sx = tl.tl_rotate_quant_act(_dev(L.x_bits.view(np.int16), torch.bfloat16), xq_dtype=tl.TL_F16)
     acc_ref = torch.empty((M, N), dtype=torch.int32, device="cuda")
-    ws = torch.zeros((need,), dtype=torch.uint8, device="cuda")
-    tl.tl_linear_prefill(packed, qT, sw, xq, sx, N, K, tl.TL_F32, acc_dbg=acc_ref, workspace=ws)
+    tl.tl_linear_prefill(packed, qT, sw, xq, sx, N, K, tl.TL_F32, acc_dbg=acc_ref)
     y = torch.empty((M, N), dtype=torch.float32, device="cuda")
     acc = torch.full((M, N), -(2 ** 31), dtype=torch.int32, device="cuda")
     assert _call_raw(tl, packed, qT, sw, xq, sx, M, N, K, y, acc) == tl.TL_OK
