@@ -307,24 +307,19 @@ class TernaryLinear:
     """
 
     # Which kernel serves a batch of M tokens (measured on GB300 over both MLP
-    # shapes, K = 5120 and 17408, 8 layer buffers in a CUDA graph): the dp4a
-    # CUDA-core decode up to 4 tokens; the mma.sync tensor-core decode for 5 to
-    # 16 tokens while K <= 8192 (M = 8: 16.6 against 20.0 us for dp4a and 20.9
-    # for the prefill kernel; M = 16: the kernels tie at 21.5 us, the layer with
-    # its rotation takes 24.0 against 25.5 us); the tcgen05 prefill kernel above,
-    # and from 5 tokens at deeper K (K = 17408, M = 5..16: 20.5-20.8 against
-    # 24.1-32.8 us for the tensor-core decode).
+    # shapes, rotate+quantise and the kernel per layer, 8 layer buffers in a
+    # CUDA graph): the dp4a CUDA-core decode up to 4 tokens while M K <= 64 K
+    # (K = 5120, M = 4: 16.2 against 17.2 us for the prefill kernel; K = 17408,
+    # M = 3: 21.5 against 21.6, M = 4: 22.5 against 21.8); the tcgen05 prefill
+    # kernel above (K = 5120, M = 5..16: 17.3 us against 18.2-23.4 for the
+    # mma.sync tensor-core decode, which tl_linear_decode_tc still offers).
     DECODE_MAX_M = 4
-    DECODE_MAX_MK = 72 * 1024
-    TC_MAX_M = 16
-    TC_MAX_K = 8192
+    DECODE_MAX_MK = 64 * 1024
 
     def kernel_for(self, M: int) -> str:
-        """'decode', 'decode_tc' or 'prefill': the kernel forward() runs for M tokens."""
+        """'decode' or 'prefill': the kernel forward() runs for M tokens."""
         if M <= self.DECODE_MAX_M and M * self.K <= self.DECODE_MAX_MK:
             return "decode"
-        if M <= self.TC_MAX_M and self.K <= self.TC_MAX_K:
-            return "decode_tc"
         return "prefill"
 
     def __init__(self, codes: torch.Tensor, s: torch.Tensor, device="cuda", y_dtype: int = TL_BF16):
@@ -357,10 +352,6 @@ class TernaryLinear:
             xq, sx = tl_rotate_quant_act(xd, xq_dtype=TL_I8, stream=stream)
             y = tl_linear_decode(self.packed, self.qT, self.sw, xq, sx, self.N, self.K,
                                  self.y_dtype, y=out, stream=stream)
-        elif kind == "decode_tc":
-            xq, sx = tl_rotate_quant_act(xd, xq_dtype=TL_F16, stream=stream)
-            y = tl_linear_decode_tc(self.packed, self.qT, self.sw, xq, sx, self.N, self.K,
-                                    self.y_dtype, y=out, stream=stream)
         else:
             xq, sx = tl_rotate_quant_act(xd, xq_dtype=TL_F16, stream=stream)
             y = tl_linear_prefill(self.packed, self.qT, self.sw, xq, sx, self.N, self.K,

@@ -618,11 +618,11 @@ def test_argument_errors_launch_nothing(tl):
 
 
 @pytest.mark.parametrize("K", [5120, 17408])
-@pytest.mark.parametrize("M", [1, 4, 5, 12, 16, 17, 40])
+@pytest.mark.parametrize("M", [1, 3, 4, 5, 12, 16, 17, 40])
 def test_forward_every_route(tl, M, K):
-    """TernaryLinear.forward on each side of each kernel boundary (dp4a decode,
-    tensor-core decode, prefill) matches the oracle: bf16 y within one ulp of
-    the oracle's, f32 y identical."""
+    """TernaryLinear.forward on each side of its kernel boundary (dp4a decode,
+    prefill) matches the oracle: bf16 y within one ulp of the oracle's, f32 y
+    identical."""
     L = synth.config_inputs("decode", M=M, N=384, K=K)
     lay = tl.TernaryLinear(torch.from_numpy(L.codes), torch.from_numpy(L.s))
     lay32 = tl.TernaryLinear(torch.from_numpy(L.codes), torch.from_numpy(L.s), y_dtype=tl.TL_F32)
