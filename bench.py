@@ -606,7 +606,9 @@ def main(argv=None):
                          "peak": hbm_peak, "unit": "GB/s",
                          "frac": wb / (m16_kernel_us * 1e-6) / 1e9 / hbm_peak,
                          "peak_source": f"{peak_src} hbm_gbs",
-                         "floor_us": wb / hbm_peak / 1e3},
+                         "floor_us": wb / hbm_peak / 1e3,
+                         "traffic": traffic.get("prefill_kernel_narrow_M16" if kind16 == "prefill"
+                                                else "decode_tc_kernel")},
         },
         "decode_f32act": {
             "metric": "float-activation decode GEMV weight-stream GB/s @M=1",
