@@ -548,6 +548,36 @@ def _sample_rows(N, n=192, seed=0):
     return np.sort(rng.choice(N, size=n, replace=False))
 
 
+@pytest.mark.parametrize("M,N,K", [pytest.param(128, 80 * 128, 17408, id="regions"),
+                                   pytest.param(64, 256, 17408, id="atomics"),
+                                   pytest.param(1024, 5120, 17408, id="atomics-last-round")])
+def test_prefill_cut_tiles_match_whole_tiles(tl, M, N, K):
+    """A tile cut along K between CTAs meets through one region per CTA (at most three CTAs
+    per tile: 80 tiles of 17 chunks over 152 SMs) or through atomics into one region (more
+    CTAs per tile; the 1024-token case cuts only the last partial round of SMs): the int32
+    result equals the one with every tile whole (no workspace), and the call leaves the
+    workspace zero."""
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    need = tl.tl_prefill_workspace_size(M, N, K)
+    if need == 0:
+        pytest.skip(f"with {sms} SMs this shape is not cut")
+    codes, s, x = synth.torch_layer(7, M, K, N, p0=0.4, mu=-4.0, sigma=0.5, x_kind="t3")
+    packed, qT, sw = tl.tl_pack_weights(codes, s)
+    del codes
+    xq, sx = tl.tl_rotate_quant_act(x, xq_dtype=tl.TL_F16)
+    ws = torch.zeros((need,), dtype=torch.uint8, device="cuda")
+    a_cut = torch.full((M, N), ACC_SENTINEL, dtype=torch.int32, device="cuda")
+    a_whole = torch.full((M, N), ACC_SENTINEL, dtype=torch.int32, device="cuda")
+    for _ in range(2):   # the second call reuses the workspace the first one returned to zero
+        y_cut = tl.tl_linear_prefill(packed, qT, sw, xq, sx, N, K, tl.TL_F32, acc_dbg=a_cut, workspace=ws)
+        check_status(tl)
+        assert not torch.any(ws)
+    y_whole = tl.tl_linear_prefill(packed, qT, sw, xq, sx, N, K, tl.TL_F32, acc_dbg=a_whole)
+    check_status(tl)
+    assert not torch.any(a_cut == ACC_SENTINEL)
+    assert torch.equal(a_cut, a_whole) and torch.equal(y_cut, y_whole)
+
+
 @pytest.mark.parametrize("name,path", [("decode", "decode"), ("decode16", "decode"),
                                        ("down_proj", "prefill"), ("gate_up", "prefill")])
 def test_full_size_sampled(tl, name, path):
