@@ -343,7 +343,12 @@ class TernaryLinear:
         return self._ws
 
     def forward(self, x: torch.Tensor, stream=None, out: torch.Tensor | None = None) -> torch.Tensor:
-        """y = layer(x). `out` (device, [M, N], the layer's y dtype) receives y when given."""
+        """y = layer(x). `out` (device, [M, N], the layer's y dtype) receives y when given.
+
+        The layer keeps one split-K workspace for the prefill kernel (used when a
+        batch has few output tiles and a long K): calls on the same layer object
+        that can run at the same time on different streams must be ordered by
+        the caller (an event), or use one layer object per stream."""
         on_host = not x.is_cuda
         xd = x.to(self.device, non_blocking=True) if on_host else x
         M = xd.shape[0]
